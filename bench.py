@@ -1,0 +1,429 @@
+#!/usr/bin/env python3
+"""Throughput benchmark of the pipelined GEMMs on GB300.
+
+Default workload (one GPU): fp32 SGEMM M = N = K = 4096, row-major, A, B and
+the initial C uniform in [-1, 1) from a fixed seed, alpha = 1, beta = 0.5 --
+the FFMA path.  The bf16 8192^3 and int8 4096^3 workloads are measured in the
+same run and reported under "also".
+
+A step is one library call C <- alpha*A*B + beta*C on operands already
+resident in HBM.  Between timed steps L2 is flushed by writing a buffer larger
+than L2, and each step is timed with CUDA events on the launching stream;
+the K timed steps are bracketed by a barrier and a device synchronise, and the
+reported time is the maximum over ranks.
+
+``e2e`` times the same call end to end: the pinned host operands are copied to
+the device, the GEMM runs, and C is copied back, every step.
+
+``--impl reference`` times the CPU oracle (the reference arm of this
+comparison) on the host cores, on a bounded sample of the same workload.
+
+With N > 1 (torchrun) every rank runs an independent replica on its own GPU
+(the GEMM is not partitioned across GPUs); ``value`` is the FLOPs of all ranks
+divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import seeded_inputs as si  # noqa: E402
+
+METRIC = "GEMM TFLOP/s (TOP/s int8) at 4096-8192^3 and % of GB300 dtype peak, 1 GPU"
+
+# name -> (dtype, M, N, K, recipe, seed)
+WORKLOADS = {
+    "sgemm_fp32_4096": ("f32", 4096, 4096, 4096, "f32_uniform_beta", si.config_seed(2)),
+    "igemm_i8_4096": ("i8", 4096, 4096, 4096, "i8_uniform", si.config_seed(3)),
+    "gemm_bf16_8192": ("bf16", 8192, 8192, 8192, "bf16_normal", si.config_seed(4)),
+}
+DEFAULT_WORKLOAD = "sgemm_fp32_4096"
+L2_FLUSH_BYTES = 512 << 20  # > 129 MB of L2
+
+
+# ------------------------------------------------------------------ peaks ---
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "sm_max_mhz": 2070.0, "source": "fallback"}
+
+
+def ffma_peak_tflops(sm_count: int, mhz: float) -> float:
+    """FP32 FFMA peak: SMs x 128 FP32 lanes x 2 FLOP per FMA x clock."""
+    return sm_count * 128 * 2 * mhz * 1e6 / 1e12
+
+
+def roofline_for(dtype: str, achieved_tflops: float, sm_count: int, peaks: dict) -> dict:
+    if dtype == "f32":
+        peak = ffma_peak_tflops(sm_count, float(peaks.get("sm_max_mhz", 2070.0)))
+        return {"bound": "alu", "achieved": round(achieved_tflops, 2), "peak": round(peak, 2),
+                "unit": "TFLOP/s", "frac": round(achieved_tflops / peak, 4),
+                "peak_source": f"derived: {sm_count} SMs x 128 FP32 lanes x 2 x "
+                               f"{peaks.get('sm_max_mhz', 2070.0)} MHz"}
+    # bf16, and int8 run as fp16 on the same kind::f16 tensor pipe (same nominal rate)
+    peak = float(peaks["bf16_tflops"])
+    return {"bound": "tensor", "achieved": round(achieved_tflops, 2), "peak": peak,
+            "unit": "TFLOP/s" if dtype == "bf16" else "TOP/s",
+            "frac": round(achieved_tflops / peak, 4),
+            "peak_source": f"{peaks['source']} bf16 dense (burst)" +
+                           ("; int8 runs as exact fp16 products on the same pipe" if dtype == "i8" else "")}
+
+
+def traffic_for(kernel_key: str):
+    """DRAM bytes per launch from the committed ncu summary, or None if the
+    kernel source changed since it was captured."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel_key)
+    if not e or e.get("source_sha") != kernel_source_sha():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "software_pipelined_tiled_loop_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+# ----------------------------------------------------------------- clocks ---
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ GPU arm ---
+def _torch_dtype(torch, np_dtype):
+    return {np.float32: torch.float32, np.int8: torch.int8, np.int32: torch.int32,
+            np.uint16: torch.int16}[np.dtype(np_dtype).type]
+
+
+def _to_dev(torch, x):
+    if x.dtype == np.uint16:
+        x = x.view(np.int16)
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+def run_gpu_workload(name: str, steps: int, warmup: int, dist_ctx, with_e2e: bool) -> dict:
+    import torch
+
+    import software_pipelined_tiled_loop_gb300 as pg
+
+    dtype, M, N, K, recipe, seed = WORKLOADS[name]
+    A, B, C0, alpha, beta, _ = si.workload(recipe, M, N, K, seed)
+    fn = {"f32": pg.gemm_f32, "bf16": pg.gemm_bf16, "i8": pg.gemm_i8}[dtype]
+    dA, dB, dC = _to_dev(torch, A), _to_dev(torch, B), _to_dev(torch, C0)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    flops = 2.0 * M * N * K
+
+    for _ in range(warmup):
+        fn(M, N, K, alpha, dA, dB, beta, dC)
+    torch.cuda.synchronize()
+    if pg.pgemm_get_device_status() != 0:
+        raise RuntimeError("device status after warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    dist_ctx.barrier()
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush.fill_(float(i))  # evict A, B, C from L2 between timed steps
+        starts[i].record(stream)
+        fn(M, N, K, alpha, dA, dB, beta, dC)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    dist_ctx.barrier()
+    per_step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    if pg.pgemm_get_device_status() != 0:
+        raise RuntimeError("device status after timed steps")
+    total_ms = dist_ctx.max(sum(per_step_ms))
+    res = {"dtype": dtype, "M": M, "N": N, "K": K, "alpha": alpha, "beta": beta,
+           "ms_per_step": total_ms / steps, "ms_min": min(per_step_ms),
+           "ms_median": statistics.median(per_step_ms),
+           "tflops": flops * steps * dist_ctx.world / (total_ms * 1e-3) / 1e12,
+           "per_gpu_tflops": flops * steps / (total_ms * 1e-3) / 1e12,
+           "launches_per_step": 1 if dtype != "i8" else 3,
+           "config": pg.pgemm_default_config(dtype, M, N, K)}
+
+    if with_e2e:
+        # end to end through the public call: pinned host -> device, GEMM, C -> host
+        hA = torch.from_numpy(A.view(np.int16) if A.dtype == np.uint16 else A).pin_memory()
+        hB = torch.from_numpy(B.view(np.int16) if B.dtype == np.uint16 else B).pin_memory()
+        hC = torch.from_numpy(C0).pin_memory()
+        hOut = torch.empty_like(hC).pin_memory()
+        e_steps = max(3, min(steps, 10))
+        for _ in range(2):
+            dA.copy_(hA, non_blocking=True)
+            dB.copy_(hB, non_blocking=True)
+            dC.copy_(hC, non_blocking=True)
+            fn(M, N, K, alpha, dA, dB, beta, dC)
+            hOut.copy_(dC, non_blocking=True)
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        dist_ctx.barrier()
+        torch.cuda.synchronize()
+        t0.record(stream)
+        for _ in range(e_steps):
+            dA.copy_(hA, non_blocking=True)
+            dB.copy_(hB, non_blocking=True)
+            dC.copy_(hC, non_blocking=True)
+            fn(M, N, K, alpha, dA, dB, beta, dC)
+            hOut.copy_(dC, non_blocking=True)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        dist_ctx.barrier()
+        e_ms = dist_ctx.max(t0.elapsed_time(t1))
+        h2d = A.nbytes + B.nbytes + C0.nbytes
+        res["e2e"] = {"value": round(flops * e_steps * dist_ctx.world / (e_ms * 1e-3) / 1e12, 3),
+                      "unit": "TFLOP/s" if dtype != "i8" else "TOP/s",
+                      "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(C0.nbytes),
+                      "steps": e_steps, "ms_per_step": round(e_ms / e_steps, 4)}
+    del dA, dB, dC, flush
+    torch.cuda.empty_cache()
+    return res
+
+
+# ------------------------------------------------------------- CPU oracle ---
+def oracle_sample(name: str, target_s: float) -> dict:
+    """Time the oracle, as it stands, on a bounded sample (whole rows) of the
+    workload on the host cores; return throughput in the metric's unit."""
+    import oracle
+
+    dtype, M, N, K, recipe, seed = WORKLOADS[name]
+    A, B, C0, alpha, beta, _ = si.workload(recipe, M, N, K, seed)
+    orc = oracle.get()
+    threads = orc.num_threads()
+    rows = max(1, threads)
+    t0 = time.perf_counter()
+    orc.gemm(dtype, A, B, C0, alpha, beta, rows=(0, rows))
+    dt = time.perf_counter() - t0
+    # scale the sample to about target_s seconds of CPU work
+    rows2 = int(min(M, max(rows, rows * target_s / max(dt, 1e-6))))
+    t0 = time.perf_counter()
+    orc.gemm(dtype, A, B, C0, alpha, beta, rows=(0, rows2))
+    dt2 = time.perf_counter() - t0
+    flops = 2.0 * rows2 * N * K
+    return {"value": round(flops / dt2 / 1e12, 6), "unit": "TFLOP/s" if dtype != "i8" else "TOP/s",
+            "cores": threads, "kind": "oracle",
+            "sample": f"{rows2} of {M} output rows of the {name} workload "
+                      f"({rows2}x{N}x{K}, {dt2:.1f} s)",
+            "seconds": round(dt2, 2)}
+
+
+# ------------------------------------------------------------ distributed ---
+class DistCtx:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch
+            import torch.distributed as dist
+            torch.cuda.set_device(self.local_rank)
+            dist.init_process_group("nccl")
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, v: float) -> float:
+        if not self.pg:
+            return v
+        import torch
+        t = torch.tensor([v], dtype=torch.float64, device="cuda")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ------------------------------------------------------------------- main ---
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["pgemm", "reference"], default="pgemm")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-also", action="store_true", help="skip the other workloads")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="CPU work of the oracle sample (cpu_baseline / reference arm)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+
+    dtype, M, N, K, recipe, seed = WORKLOADS[args.workload]
+    config = {"workload": args.workload, "dtype": dtype, "M": M, "N": N, "K": K,
+              "recipe": recipe, "seed": seed, "l2": "flushed between timed steps (512 MiB write)"}
+
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        if rank != 0:
+            return
+        per = []
+        for _ in range(args.warmup):
+            pass  # the oracle has no warm-up state; each step is a full sample
+        sample = None
+        for _ in range(args.steps):
+            sample = oracle_sample(args.workload, max(1.0, args.cpu_seconds / args.steps))
+            per.append(sample["value"])
+        value = statistics.median(per)
+        line = {"metric": METRIC, "value": value, "unit": sample["unit"], "impl": "reference",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": {"f32": "f32", "bf16": "bf16", "i8": "int8"}[dtype],
+                "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": value, "unit": sample["unit"], "cores": sample["cores"],
+                                 "kind": "oracle", "sample": sample["sample"]},
+                "e2e": {"value": value, "unit": sample["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+
+    ctx = DistCtx()
+    import software_pipelined_tiled_loop_gb300 as pg
+    from software_pipelined_tiled_loop_gb300 import build as pgbuild
+    if ctx.rank == 0:
+        pgbuild.build()
+    ctx.barrier()
+    pg.lib()
+    peaks = measured_peaks()
+    sm_count = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(ctx.local_rank)).split(",")[0] or 0) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES", "").replace(",", "").isdigit() else ctx.local_rank
+
+    clocks = ClockSampler(gpu_index)
+    clocks.start()
+    main_res = run_gpu_workload(args.workload, args.steps, args.warmup, ctx, with_e2e=True)
+    clk = clocks.stop()
+
+    also = {}
+    if not args.no_also:
+        for other in WORKLOADS:
+            if other == args.workload:
+                continue
+            r = run_gpu_workload(other, max(5, args.steps // 2), args.warmup, ctx, with_e2e=False)
+            also[other] = {"value": round(r["tflops"], 2),
+                           "unit": "TOP/s" if r["dtype"] == "i8" else "TFLOP/s",
+                           "ms_per_step": round(r["ms_per_step"], 4),
+                           "roofline": roofline_for(r["dtype"], r["per_gpu_tflops"], sm_count, peaks),
+                           "config": r["config"]}
+
+    cpu = None
+    if ctx.rank == 0 and ctx.world == 1:
+        cpu = oracle_sample(args.workload, args.cpu_seconds)
+
+    if ctx.rank == 0:
+        roof = roofline_for(dtype, main_res["per_gpu_tflops"], sm_count, peaks)
+        roof["traffic"] = traffic_for(f"{args.workload}")
+        roof["timing"] = "CUDA events around each call on the launching stream, L2 flushed between"
+        unit = "TOP/s" if dtype == "i8" else "TFLOP/s"
+        line = {
+            "metric": METRIC, "value": round(main_res["tflops"], 3), "unit": unit,
+            "n_gpus": ctx.world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(main_res["ms_per_step"], 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": {"f32": "f32", "bf16": "bf16", "i8": "int8"}[dtype],
+            "data": "synthetic (seeded; see DESIGN.md input recipe)",
+            "config": {**config, "tile_stages": main_res["config"],
+                       "parallelism": "replicas" if ctx.world > 1 else "single"},
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": main_res.get("e2e"),
+            "gpu_launches": main_res["launches_per_step"] * args.steps,
+            "clocks": {"sm_mhz": clk.get("sm_mhz"), "sm_max_mhz": clk.get("sm_max_mhz"),
+                       "reasons": clk.get("reasons")},
+            "also": also,
+        }
+        print(json.dumps(line))
+    ctx.close()
+
+
+if __name__ == "__main__":
+    main()

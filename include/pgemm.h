@@ -1,0 +1,150 @@
+/*
+ * pgemm -- software-pipelined dense GEMM for one GB300 GPU (sm_103a).
+ *
+ * Every gemm_* call computes
+ *
+ *     C <- alpha * A * B + beta * C
+ *
+ * with row-major operands: A is M x K (leading dimension K), B is K x N
+ * (leading dimension N), C is M x N (leading dimension N).  This is the
+ * argument list, the operand walk and the alpha/beta output update of the
+ * double-buffered SGEMM in "Double Buffering: Software Pipelining the K-Loop"
+ * (section "The Kernel"), extended with a CUDA stream.  Its K-loop is
+ * software-pipelined over an S-stage shared-memory ring with a prologue, a
+ * circular steady state and a drain ("Software pipelines and asynchronous
+ * copies", sections "Prologue, steady state, and epilogue" and
+ * "Producer-consumer synchronization"): TMA bulk-tensor copies fill a stage
+ * and complete on its "full" mbarrier (readiness edge); the consumers release
+ * it through its "empty" mbarrier (reuse edge).
+ *
+ * Common rules for all gemm_* entry points:
+ *   - A, B and C are DEVICE pointers owned by the caller; the library keeps no
+ *     reference after the call returns.  C is read (when beta != 0) and
+ *     written in place.  A and C, or B and C, must not overlap.
+ *   - The call is asynchronous on `stream` (NULL = the legacy default
+ *     stream): it enqueues work and returns; the caller synchronises.  The
+ *     library may enqueue a small repack kernel and stream-ordered scratch
+ *     (cudaMallocAsync / cudaFreeAsync) on the same stream when a leading
+ *     dimension is not a multiple of 16 bytes.
+ *   - M, N, K >= 0.  M == 0 or N == 0: nothing is done.  K == 0: C <- beta*C
+ *     (C is not read when beta == 0, so a NaN in C does not survive).
+ *   - beta == 0: C is not read (BLAS convention).
+ *   - Errors are returned synchronously: PGEMM_ERR_INVALID_VALUE (negative
+ *     dimension, NULL pointer with a non-empty operand, bad config),
+ *     PGEMM_ERR_MISALIGNED (a base pointer not 16-byte aligned),
+ *     PGEMM_ERR_UNSUPPORTED_DEVICE (the current device is not sm_103),
+ *     PGEMM_ERR_CUDA (a launch or runtime failure; the CUDA error is also
+ *     left for cudaGetLastError).  A device-side wait that ran past its time
+ *     limit is not visible here; pgemm_get_device_status() reports it.
+ *   - Thread safety: calls may come from several host threads; the first
+ *     call on a device does a one-time set-up.
+ */
+#ifndef PGEMM_H
+#define PGEMM_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PGEMM_API __attribute__((visibility("default")))
+#else
+#define PGEMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The same type as cudaStream_t (a pointer to the runtime's stream object). */
+typedef struct CUstream_st *pgemm_stream_t;
+
+typedef enum {
+    PGEMM_OK = 0,
+    PGEMM_ERR_INVALID_VALUE = 1,
+    PGEMM_ERR_MISALIGNED = 2,
+    PGEMM_ERR_UNSUPPORTED_DEVICE = 3,
+    PGEMM_ERR_CUDA = 4,
+    PGEMM_ERR_TIMEOUT = 5,
+    PGEMM_ERR_UNSUPPORTED_CONFIG = 6
+} pgemm_status;
+
+/* Data types, for the introspection calls. */
+typedef enum { PGEMM_F32 = 0, PGEMM_BF16 = 1, PGEMM_I8 = 2 } pgemm_dtype;
+
+/* A kernel configuration: output tile bm x bn, K-tile bk (elements), and the
+ * number of pipeline stages (shared-memory ring slots).  Stage count trades
+ * latency coverage against shared memory and resident blocks ("Software
+ * pipelines and asynchronous copies", section "Selecting the number of
+ * stages").  Zero fields mean "library default for this shape". */
+typedef struct {
+    int bm, bn, bk, stages;
+} pgemm_config;
+
+/* fp32: FFMA register-tiled consumers on the pipelined ring.  Semantics are
+ * plain fp32 multiply-add (no TF32).  Alignment: A, B, C 16-byte aligned.
+ * Any M, N, K (tails and unaligned leading dimensions are handled). */
+PGEMM_API pgemm_status gemm_f32(int M, int N, int K, float alpha, const float *A, const float *B,
+                      float beta, float *C, pgemm_stream_t stream);
+
+/* bf16: A and B hold bf16 bit patterns (uint16); products are accumulated in
+ * fp32 in tensor memory (tcgen05.mma kind::f16) and C is fp32.  alpha and
+ * beta are fp32. */
+PGEMM_API pgemm_status gemm_bf16(int M, int N, int K, float alpha, const uint16_t *A, const uint16_t *B,
+                       float beta, float *C, pgemm_stream_t stream);
+
+/* int8: A, B int8; the exact integer dot products are accumulated modulo 2^32
+ * into int32; C <- alpha*acc + beta*C in int32 arithmetic modulo 2^32 (two's
+ * complement wrap-around).  The products run on the tensor cores as fp16
+ * values (exact for |v| <= 128) with exact fp32 partial sums over K chunks of
+ * at most 256, folded into int32. */
+PGEMM_API pgemm_status gemm_i8(int M, int N, int K, int32_t alpha, const int8_t *A, const int8_t *B,
+                     int32_t beta, int32_t *C, pgemm_stream_t stream);
+
+/* The same three operations with an explicit configuration (cfg may be NULL
+ * for the default).  Returns PGEMM_ERR_UNSUPPORTED_CONFIG for a configuration
+ * the library was not built with (pgemm_list_configs enumerates them). */
+PGEMM_API pgemm_status gemm_f32_ex(int M, int N, int K, float alpha, const float *A, const float *B,
+                         float beta, float *C, const pgemm_config *cfg, pgemm_stream_t stream);
+PGEMM_API pgemm_status gemm_bf16_ex(int M, int N, int K, float alpha, const uint16_t *A,
+                          const uint16_t *B, float beta, float *C, const pgemm_config *cfg,
+                          pgemm_stream_t stream);
+PGEMM_API pgemm_status gemm_i8_ex(int M, int N, int K, int32_t alpha, const int8_t *A, const int8_t *B,
+                        int32_t beta, int32_t *C, const pgemm_config *cfg, pgemm_stream_t stream);
+
+/* The configuration the library picks for a shape (the per-shape table). */
+PGEMM_API pgemm_status pgemm_default_config(pgemm_dtype dtype, int M, int N, int K, pgemm_config *out);
+
+/* Up to `cap` built configurations of a dtype written to `out`; returns how
+ * many exist (call with cap = 0 to count). */
+PGEMM_API int pgemm_list_configs(pgemm_dtype dtype, pgemm_config *out, int cap);
+
+/* Resource figures of one configuration's kernel on the current device:
+ * dynamic shared memory per block (bytes), registers per thread, threads per
+ * block and resident blocks per SM.  Any output pointer may be NULL. */
+PGEMM_API pgemm_status pgemm_kernel_attrs(pgemm_dtype dtype, const pgemm_config *cfg, int *smem_bytes,
+                                int *regs_per_thread, int *threads_per_block,
+                                int *blocks_per_sm);
+
+/* Synchronises `stream`, then reads and clears the library's device status
+ * word of the current device: PGEMM_OK, or PGEMM_ERR_TIMEOUT if a kernel's
+ * bounded mbarrier wait ran out (the kernel then skipped the rest of its work
+ * and returned; its output is undefined).  PGEMM_ERR_CUDA on a CUDA error. */
+PGEMM_API pgemm_status pgemm_get_device_status(pgemm_stream_t stream);
+
+/* A self-test of the bounded-wait path: launches one block that waits, with a
+ * time limit of `limit_us` microseconds, on an mbarrier that nothing will
+ * ever arrive on, and returns what pgemm_get_device_status then reports
+ * (PGEMM_ERR_TIMEOUT when the wait path works).  The kernel never hangs and
+ * never faults; the context stays usable. */
+PGEMM_API pgemm_status pgemm_selftest_wait_timeout(int limit_us, pgemm_stream_t stream);
+
+/* A static description of a status code. */
+PGEMM_API const char *pgemm_status_string(pgemm_status status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+PGEMM_API int pgemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PGEMM_H */

@@ -1,0 +1,214 @@
+"""Python binding of libpipegemm, the software-pipelined GEMM library for GB300.
+
+Argument marshalling only: every function here forwards to the C ABI declared
+in ``include/pgemm.h`` (same names), and all arithmetic runs in the library's
+CUDA kernels.  There is no fallback: if ``libpipegemm.so`` has not been built,
+``lib()`` raises.
+
+Operands may be given as torch tensors (CUDA, contiguous, row-major) or as raw
+device pointers (ints).  ``stream`` defaults to torch's current stream when
+torch is importable, else the legacy default stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "PgemmError", "lib", "library_path", "gemm_f32", "gemm_bf16", "gemm_i8", "gemm_f32_ex",
+    "gemm_bf16_ex", "gemm_i8_ex", "pgemm_default_config", "pgemm_list_configs",
+    "pgemm_kernel_attrs", "pgemm_get_device_status", "pgemm_selftest_wait_timeout",
+    "pgemm_status_string", "pgemm_version", "DTYPES", "STATUS", "EXPORTED",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_HERE, "libpipegemm.so")
+
+STATUS = {
+    0: "PGEMM_OK", 1: "PGEMM_ERR_INVALID_VALUE", 2: "PGEMM_ERR_MISALIGNED",
+    3: "PGEMM_ERR_UNSUPPORTED_DEVICE", 4: "PGEMM_ERR_CUDA", 5: "PGEMM_ERR_TIMEOUT",
+    6: "PGEMM_ERR_UNSUPPORTED_CONFIG",
+}
+DTYPES = {"f32": 0, "bf16": 1, "i8": 2}
+# Every function include/pgemm.h declares.
+EXPORTED = [
+    "gemm_f32", "gemm_bf16", "gemm_i8", "gemm_f32_ex", "gemm_bf16_ex", "gemm_i8_ex",
+    "pgemm_default_config", "pgemm_list_configs", "pgemm_kernel_attrs",
+    "pgemm_get_device_status", "pgemm_selftest_wait_timeout", "pgemm_status_string",
+    "pgemm_version",
+]
+
+
+class PgemmError(RuntimeError):
+    """A non-OK pgemm_status."""
+
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS.get(code, code)}")
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("bm", ctypes.c_int), ("bn", ctypes.c_int), ("bk", ctypes.c_int),
+                ("stages", ctypes.c_int)]
+
+    def as_tuple(self):
+        return (self.bm, self.bn, self.bk, self.stages)
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
+    i, f, vp, i32 = ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_int32
+    cfgp = ctypes.POINTER(Config)
+    ip = ctypes.POINTER(ctypes.c_int)
+    sig = {
+        "gemm_f32": [i, i, i, f, vp, vp, f, vp, vp],
+        "gemm_bf16": [i, i, i, f, vp, vp, f, vp, vp],
+        "gemm_i8": [i, i, i, i32, vp, vp, i32, vp, vp],
+        "gemm_f32_ex": [i, i, i, f, vp, vp, f, vp, cfgp, vp],
+        "gemm_bf16_ex": [i, i, i, f, vp, vp, f, vp, cfgp, vp],
+        "gemm_i8_ex": [i, i, i, i32, vp, vp, i32, vp, cfgp, vp],
+        "pgemm_default_config": [i, i, i, i, cfgp],
+        "pgemm_list_configs": [i, cfgp, i],
+        "pgemm_kernel_attrs": [i, cfgp, ip, ip, ip, ip],
+        "pgemm_get_device_status": [vp],
+        "pgemm_selftest_wait_timeout": [i, vp],
+        "pgemm_status_string": [i],
+        "pgemm_version": [],
+    }
+    for name, args in sig.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    L.pgemm_status_string.restype = ctypes.c_char_p
+    return L
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library.  Raises if it has not been built (no fallback)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(library_path):
+                raise RuntimeError(
+                    f"{library_path} is missing: build it with "
+                    "`python -m software_pipelined_tiled_loop_gb300.build` (needs nvcc)")
+            _lib = _declare(ctypes.CDLL(library_path))
+        return _lib
+
+
+def _ptr(x) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        if not x.is_cuda:
+            raise ValueError("operands must be CUDA tensors (or raw device pointers)")
+        if not x.is_contiguous():
+            raise ValueError("operands must be contiguous row-major tensors")
+        return int(x.data_ptr())
+    raise TypeError(f"cannot take a device pointer from {type(x).__name__}")
+
+
+def _stream(s) -> int:
+    if s is None:
+        try:
+            import torch
+            if torch.cuda.is_available():
+                return int(torch.cuda.current_stream().cuda_stream)
+        except ImportError:
+            pass
+        return 0
+    if isinstance(s, int):
+        return s
+    return int(s.cuda_stream)
+
+
+def _check(code: int, where: str) -> None:
+    if code != 0:
+        raise PgemmError(code, where)
+
+
+def _cfg(config):
+    if config is None:
+        return None
+    if isinstance(config, Config):
+        return ctypes.byref(config)
+    bm, bn, bk, stages = config
+    return ctypes.byref(Config(bm, bn, bk, stages))
+
+
+def gemm_f32(M, N, K, alpha, A, B, beta, C, stream=None):
+    """C <- alpha*A@B + beta*C, fp32 (FFMA).  Asynchronous on ``stream``."""
+    _check(lib().gemm_f32(M, N, K, alpha, _ptr(A), _ptr(B), beta, _ptr(C), _stream(stream)),
+           "gemm_f32")
+
+
+def gemm_bf16(M, N, K, alpha, A, B, beta, C, stream=None):
+    """C (fp32) <- alpha*A@B + beta*C with bf16 A, B (tcgen05).  Asynchronous."""
+    _check(lib().gemm_bf16(M, N, K, alpha, _ptr(A), _ptr(B), beta, _ptr(C), _stream(stream)),
+           "gemm_bf16")
+
+
+def gemm_i8(M, N, K, alpha, A, B, beta, C, stream=None):
+    """C (int32) <- alpha*A@B + beta*C with int8 A, B, exact modulo 2^32.  Asynchronous."""
+    _check(lib().gemm_i8(M, N, K, int(alpha), _ptr(A), _ptr(B), int(beta), _ptr(C),
+                         _stream(stream)), "gemm_i8")
+
+
+def gemm_f32_ex(M, N, K, alpha, A, B, beta, C, config=None, stream=None):
+    _check(lib().gemm_f32_ex(M, N, K, alpha, _ptr(A), _ptr(B), beta, _ptr(C), _cfg(config),
+                             _stream(stream)), "gemm_f32_ex")
+
+
+def gemm_bf16_ex(M, N, K, alpha, A, B, beta, C, config=None, stream=None):
+    _check(lib().gemm_bf16_ex(M, N, K, alpha, _ptr(A), _ptr(B), beta, _ptr(C), _cfg(config),
+                              _stream(stream)), "gemm_bf16_ex")
+
+
+def gemm_i8_ex(M, N, K, alpha, A, B, beta, C, config=None, stream=None):
+    _check(lib().gemm_i8_ex(M, N, K, int(alpha), _ptr(A), _ptr(B), int(beta), _ptr(C),
+                            _cfg(config), _stream(stream)), "gemm_i8_ex")
+
+
+def pgemm_default_config(dtype: str, M: int, N: int, K: int):
+    c = Config()
+    _check(lib().pgemm_default_config(DTYPES[dtype], M, N, K, ctypes.byref(c)),
+           "pgemm_default_config")
+    return c.as_tuple()
+
+
+def pgemm_list_configs(dtype: str):
+    n = lib().pgemm_list_configs(DTYPES[dtype], None, 0)
+    arr = (Config * max(n, 1))()
+    lib().pgemm_list_configs(DTYPES[dtype], arr, n)
+    return [arr[i].as_tuple() for i in range(n)]
+
+
+def pgemm_kernel_attrs(dtype: str, config):
+    out = [ctypes.c_int(0) for _ in range(4)]
+    _check(lib().pgemm_kernel_attrs(DTYPES[dtype], _cfg(config), *[ctypes.byref(o) for o in out]),
+           "pgemm_kernel_attrs")
+    return {"smem_bytes": out[0].value, "regs_per_thread": out[1].value,
+            "threads_per_block": out[2].value, "blocks_per_sm": out[3].value}
+
+
+def pgemm_get_device_status(stream=None) -> int:
+    """Synchronise ``stream`` and return (and clear) the device status code."""
+    return int(lib().pgemm_get_device_status(_stream(stream)))
+
+
+def pgemm_selftest_wait_timeout(limit_us: int, stream=None) -> int:
+    return int(lib().pgemm_selftest_wait_timeout(int(limit_us), _stream(stream)))
+
+
+def pgemm_status_string(code: int) -> str:
+    return lib().pgemm_status_string(int(code)).decode()
+
+
+def pgemm_version() -> int:
+    return int(lib().pgemm_version())

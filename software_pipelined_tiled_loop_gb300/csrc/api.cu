@@ -1,0 +1,457 @@
+// Host dispatch for the pipelined GEMMs: argument validation, the per-shape
+// (tile, stages) table, operand repacking for leading dimensions that TMA
+// cannot describe, tensor-map encoding and the launch on the caller's stream.
+//
+// The entry points follow the kernel signature (M, N, K, alpha, A, B, beta, C)
+// of "Double Buffering: Software Pipelining the K-Loop" (section "The
+// Kernel") plus a stream; the stage-count choice follows "Software pipelines
+// and asynchronous copies" (section "Selecting the number of stages"): a
+// deeper ring hides more latency but costs shared memory and resident blocks,
+// so the default table is per shape and every built configuration can be
+// selected explicitly for a sweep.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <unordered_map>
+
+#include "../../include/pgemm.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace pg {
+
+// The device status word of each device (one instance per device context).
+__device__ uint32_t g_status_word = 0;
+
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s per mbarrier wait
+constexpr int kMaxDevices = 64;
+
+struct KernelState {
+    bool ready = false;
+    int blocks_per_sm = 0;
+};
+
+struct DeviceState {
+    bool init = false;
+    pgemm_status init_status = PGEMM_OK;
+    int sm_count = 0;
+    uint32_t *status = nullptr;
+    std::unordered_map<const void *, KernelState> kernels;
+};
+
+static std::mutex g_mu;
+static DeviceState g_dev[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+static EncodeTiledFn g_encode = nullptr;
+
+// One-time set-up of the current device (under g_mu).
+static pgemm_status device_setup(int *dev_out, DeviceState **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PGEMM_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return PGEMM_ERR_UNSUPPORTED_DEVICE;
+    DeviceState &d = g_dev[dev];
+    if (!d.init) {
+        d.init = true;
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            d.init_status = PGEMM_ERR_CUDA;
+        } else if (major != 10 || minor != 3) {
+            // the library carries sm_103a code only
+            d.init_status = PGEMM_ERR_UNSUPPORTED_DEVICE;
+        } else if (cudaGetSymbolAddress(reinterpret_cast<void **>(&d.status), g_status_word) !=
+                   cudaSuccess) {
+            d.init_status = PGEMM_ERR_CUDA;
+        } else if (!g_encode) {
+            cudaDriverEntryPointQueryResult q{};
+            void *fn = nullptr;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q) != cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || fn == nullptr)
+                d.init_status = PGEMM_ERR_CUDA;
+            else
+                g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+        }
+    }
+    *dev_out = dev;
+    *out = &d;
+    return d.init_status;
+}
+
+static pgemm_status kernel_setup(DeviceState &d, const KernelInfo &k, int *blocks_per_sm) {
+    KernelState &ks = d.kernels[k.func];
+    if (!ks.ready) {
+        if (cudaFuncSetAttribute(k.func, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 k.smem_bytes) != cudaSuccess)
+            return PGEMM_ERR_CUDA;
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k.func, k.threads, k.smem_bytes) !=
+            cudaSuccess)
+            return PGEMM_ERR_CUDA;
+        if (n < 1) return PGEMM_ERR_UNSUPPORTED_CONFIG;
+        ks.blocks_per_sm = n;
+        ks.ready = true;
+    }
+    *blocks_per_sm = ks.blocks_per_sm;
+    return PGEMM_OK;
+}
+
+static const KernelInfo *table_of(pgemm_dtype dt, int *count) {
+    switch (dt) {
+        case PGEMM_F32: return f32_kernels(count);
+        case PGEMM_BF16: return bf16_kernels(count);
+        case PGEMM_I8: return i8_kernels(count);
+    }
+    *count = 0;
+    return nullptr;
+}
+
+// The per-shape default (tile, stages) table.
+static pgemm_config default_config(pgemm_dtype dt, int M, int N, int K, int sm_count) {
+    (void)K;
+    pgemm_config c{128, 128, 0, 0};
+    if (dt == PGEMM_F32) {
+        c.bn = 128;
+        c.stages = 3;  // 3 x 32 KB per block: two blocks per SM
+    } else if (dt == PGEMM_BF16) {
+        const long long tiles256 = (long long)((M + 127) / 128) * ((N + 255) / 256);
+        if (tiles256 >= sm_count) {
+            c.bn = 256;
+            c.stages = 4;
+        } else {
+            c.bn = 128;
+            c.stages = 4;
+        }
+    } else {
+        c.bn = 128;
+        c.stages = 4;
+    }
+    return c;
+}
+
+static const KernelInfo *find_kernel(pgemm_dtype dt, const pgemm_config &c) {
+    int n = 0;
+    const KernelInfo *t = table_of(dt, &n);
+    for (int i = 0; i < n; ++i)
+        if (t[i].bm == c.bm && t[i].bn == c.bn && t[i].stages == c.stages &&
+            (c.bk == 0 || c.bk == t[i].bk))
+            return &t[i];
+    return nullptr;
+}
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static pgemm_status encode_2d(CUtensorMap *map, CUtensorMapDataType type, int elem_bytes,
+                              const void *base, long long inner, long long outer, long long ld,
+                              int box_x, int box_y, bool swizzle128) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * elem_bytes};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_x), static_cast<cuuint32_t>(box_y)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, type, 2, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PGEMM_OK : PGEMM_ERR_CUDA;
+}
+
+// Copies rows [0, rows) x [0, cols) of a row-major matrix with pitch `sld` to a
+// new pitch `dld` (both in elements of `eb` bytes).
+__global__ void repack_rows_kernel(const uint8_t *__restrict__ src, long long sld,
+                                   uint8_t *__restrict__ dst, long long dld, int rows, int cols,
+                                   int eb) {
+    const long long total = static_cast<long long>(rows) * cols;
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long r = i / cols, c = i - r * cols;
+        const uint8_t *s = src + (r * sld + c) * eb;
+        uint8_t *d = dst + (r * dld + c) * eb;
+        if (eb == 2)
+            *reinterpret_cast<uint16_t *>(d) = *reinterpret_cast<const uint16_t *>(s);
+        else
+            *reinterpret_cast<uint32_t *>(d) = *reinterpret_cast<const uint32_t *>(s);
+    }
+}
+
+static cudaError_t launch_repack(const void *src, long long sld, void *dst, long long dld,
+                                 int rows, int cols, int eb, int sm_count, cudaStream_t s) {
+    const long long total = static_cast<long long>(rows) * cols;
+    if (total <= 0) return cudaSuccess;
+    long long blocks = (total + 255) / 256;
+    if (blocks > static_cast<long long>(sm_count) * 8) blocks = static_cast<long long>(sm_count) * 8;
+    repack_rows_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(
+        static_cast<const uint8_t *>(src), sld, static_cast<uint8_t *>(dst), dld, rows, cols, eb);
+    return cudaGetLastError();
+}
+
+static long long round_up(long long v, long long m) { return (v + m - 1) / m * m; }
+
+// Stream-ordered scratch owned by one call.
+struct Scratch {
+    void *p = nullptr;
+    cudaStream_t s = nullptr;
+    ~Scratch() {
+        if (p) cudaFreeAsync(p, s);
+    }
+};
+
+enum class Kind { F32, BF16, I8 };
+
+template <Kind KIND, typename In, typename Sc, typename Out>
+static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const In *B, Sc beta,
+                              Out *C, const pgemm_config *cfg_in, cudaStream_t stream) {
+    if (M < 0 || N < 0 || K < 0) return PGEMM_ERR_INVALID_VALUE;
+    if (M == 0 || N == 0) return PGEMM_OK;
+    if (C == nullptr || (K > 0 && (A == nullptr || B == nullptr))) return PGEMM_ERR_INVALID_VALUE;
+    if (!aligned16(C) || (K > 0 && (!aligned16(A) || !aligned16(B)))) return PGEMM_ERR_MISALIGNED;
+    constexpr pgemm_dtype DT =
+        KIND == Kind::F32 ? PGEMM_F32 : (KIND == Kind::BF16 ? PGEMM_BF16 : PGEMM_I8);
+
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    DeviceState *d = nullptr;
+    pgemm_status st = device_setup(&dev, &d);
+    if (st != PGEMM_OK) return st;
+
+    pgemm_config c = (cfg_in && cfg_in->stages > 0) ? *cfg_in : default_config(DT, M, N, K, d->sm_count);
+    if (c.bm == 0) c.bm = 128;
+    const KernelInfo *k = find_kernel(DT, c);
+    if (!k) return PGEMM_ERR_UNSUPPORTED_CONFIG;
+    int blocks_per_sm = 0;
+    st = kernel_setup(*d, *k, &blocks_per_sm);
+    if (st != PGEMM_OK) return st;
+
+    // Operands as the kernels read them: element type, pitch, base pointer.
+    const int in_bytes = KIND == Kind::F32 ? 4 : 2;  // int8 is widened to fp16
+    const long long lda = K, ldb = N;
+    const void *a_op = A;
+    const void *b_op = B;
+    long long a_ld = lda, b_ld = ldb;
+    Scratch scratch;
+    scratch.s = stream;
+    if (K > 0) {
+        const long long align_elems = 16 / in_bytes;
+        const bool widen = KIND == Kind::I8;
+        const bool a_repack = widen || (lda * in_bytes) % 16 != 0;
+        const bool b_repack = widen || (ldb * in_bytes) % 16 != 0;
+        if (a_repack || b_repack) {
+            const long long a_ld2 = a_repack ? round_up(K, align_elems) : lda;
+            const long long b_ld2 = b_repack ? round_up(N, align_elems) : ldb;
+            const long long a_bytes = a_repack ? round_up(a_ld2 * M * in_bytes, 256) : 0;
+            const long long b_bytes = b_repack ? round_up(b_ld2 * K * in_bytes, 256) : 0;
+            if (cudaMallocAsync(&scratch.p, a_bytes + b_bytes, stream) != cudaSuccess)
+                return PGEMM_ERR_CUDA;
+            uint8_t *base = static_cast<uint8_t *>(scratch.p);
+            cudaError_t e = cudaSuccess;
+            if (a_repack) {
+                e = widen ? launch_widen_i8(reinterpret_cast<const int8_t *>(A), lda, base, a_ld2, M,
+                                            K, d->sm_count, stream)
+                          : launch_repack(A, lda, base, a_ld2, M, K, in_bytes, d->sm_count, stream);
+                a_op = base;
+                a_ld = a_ld2;
+            }
+            if (e == cudaSuccess && b_repack) {
+                e = widen ? launch_widen_i8(reinterpret_cast<const int8_t *>(B), ldb, base + a_bytes,
+                                            b_ld2, K, N, d->sm_count, stream)
+                          : launch_repack(B, ldb, base + a_bytes, b_ld2, K, N, in_bytes,
+                                          d->sm_count, stream);
+                b_op = base + a_bytes;
+                b_ld = b_ld2;
+            }
+            if (e != cudaSuccess) return PGEMM_ERR_CUDA;
+        }
+    }
+
+    // Tensor maps.  With K == 0 nothing is ever loaded; the maps then describe
+    // a 1 x 1 region of C so that they are still valid objects.
+    alignas(64) CUtensorMap ta, tb;
+    const CUtensorMapDataType tmt = KIND == Kind::F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                    : KIND == Kind::BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    if (K > 0) {
+        st = encode_2d(&ta, tmt, in_bytes, a_op, K, M, a_ld, k->a_box_x, k->a_box_y, k->a_swizzle128);
+        if (st == PGEMM_OK)
+            st = encode_2d(&tb, tmt, in_bytes, b_op, N, K, b_ld, k->b_box_x, k->b_box_y,
+                           k->b_swizzle128);
+    } else {
+        st = encode_2d(&ta, tmt, in_bytes, C, 1, 1, 16 / in_bytes, k->a_box_x, k->a_box_y,
+                       k->a_swizzle128);
+        if (st == PGEMM_OK)
+            st = encode_2d(&tb, tmt, in_bytes, C, 1, 1, 16 / in_bytes, k->b_box_x, k->b_box_y,
+                           k->b_swizzle128);
+    }
+    if (st != PGEMM_OK) return st;
+
+    cudaError_t e = cudaSuccess;
+    KernelCtx ctx{d->status, kDefaultWaitLimitNs};
+    if constexpr (KIND == Kind::F32) {
+        LaunchF32 p{};
+        p.M = M; p.N = N; p.K = K; p.ldc = N; p.group_m = 0;
+        p.sm_count = d->sm_count; p.blocks_per_sm = blocks_per_sm;
+        p.tmap_a = &ta; p.tmap_b = &tb; p.ctx = ctx;
+        p.alpha = alpha; p.beta = beta; p.C = C;
+        e = k->launch_f32(p, stream);
+    } else if constexpr (KIND == Kind::BF16) {
+        LaunchBf16 p{};
+        p.M = M; p.N = N; p.K = K; p.ldc = N; p.group_m = 0;
+        p.sm_count = d->sm_count; p.blocks_per_sm = blocks_per_sm;
+        p.tmap_a = &ta; p.tmap_b = &tb; p.ctx = ctx;
+        p.alpha = alpha; p.beta = beta; p.C = C;
+        e = k->launch_bf16(p, stream);
+    } else {
+        LaunchI8 p{};
+        p.M = M; p.N = N; p.K = K; p.ldc = N; p.group_m = 0;
+        p.sm_count = d->sm_count; p.blocks_per_sm = blocks_per_sm;
+        p.tmap_a = &ta; p.tmap_b = &tb; p.ctx = ctx;
+        p.alpha = alpha; p.beta = beta; p.C = C;
+        e = k->launch_i8(p, stream);
+    }
+    return e == cudaSuccess ? PGEMM_OK : PGEMM_ERR_CUDA;
+}
+
+// A block that waits, with a short limit, on an mbarrier nothing arrives on.
+__global__ void selftest_wait_kernel(KernelCtx ctx) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait(&bar, 0, ctx, kSiteSelfTest);
+}
+
+}  // namespace pg
+
+using namespace pg;
+
+extern "C" {
+
+pgemm_status gemm_f32(int M, int N, int K, float alpha, const float *A, const float *B, float beta,
+                      float *C, pgemm_stream_t stream) {
+    return gemm_impl<Kind::F32>(M, N, K, alpha, A, B, beta, C, nullptr, stream);
+}
+
+pgemm_status gemm_bf16(int M, int N, int K, float alpha, const uint16_t *A, const uint16_t *B,
+                       float beta, float *C, pgemm_stream_t stream) {
+    return gemm_impl<Kind::BF16>(M, N, K, alpha, A, B, beta, C, nullptr, stream);
+}
+
+pgemm_status gemm_i8(int M, int N, int K, int32_t alpha, const int8_t *A, const int8_t *B,
+                     int32_t beta, int32_t *C, pgemm_stream_t stream) {
+    return gemm_impl<Kind::I8>(M, N, K, alpha, A, B, beta, C, nullptr, stream);
+}
+
+pgemm_status gemm_f32_ex(int M, int N, int K, float alpha, const float *A, const float *B,
+                         float beta, float *C, const pgemm_config *cfg, pgemm_stream_t stream) {
+    return gemm_impl<Kind::F32>(M, N, K, alpha, A, B, beta, C, cfg, stream);
+}
+
+pgemm_status gemm_bf16_ex(int M, int N, int K, float alpha, const uint16_t *A, const uint16_t *B,
+                          float beta, float *C, const pgemm_config *cfg, pgemm_stream_t stream) {
+    return gemm_impl<Kind::BF16>(M, N, K, alpha, A, B, beta, C, cfg, stream);
+}
+
+pgemm_status gemm_i8_ex(int M, int N, int K, int32_t alpha, const int8_t *A, const int8_t *B,
+                        int32_t beta, int32_t *C, const pgemm_config *cfg, pgemm_stream_t stream) {
+    return gemm_impl<Kind::I8>(M, N, K, alpha, A, B, beta, C, cfg, stream);
+}
+
+pgemm_status pgemm_default_config(pgemm_dtype dtype, int M, int N, int K, pgemm_config *out) {
+    if (!out || M < 0 || N < 0 || K < 0) return PGEMM_ERR_INVALID_VALUE;
+    if (dtype != PGEMM_F32 && dtype != PGEMM_BF16 && dtype != PGEMM_I8) return PGEMM_ERR_INVALID_VALUE;
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    DeviceState *d = nullptr;
+    pgemm_status st = device_setup(&dev, &d);
+    if (st != PGEMM_OK) return st;
+    *out = default_config(dtype, M, N, K, d->sm_count);
+    const KernelInfo *k = find_kernel(dtype, *out);
+    if (k) out->bk = k->bk;
+    return PGEMM_OK;
+}
+
+int pgemm_list_configs(pgemm_dtype dtype, pgemm_config *out, int cap) {
+    int n = 0;
+    const KernelInfo *t = table_of(dtype, &n);
+    for (int i = 0; i < n && i < cap && out; ++i) out[i] = pgemm_config{t[i].bm, t[i].bn, t[i].bk, t[i].stages};
+    return n;
+}
+
+pgemm_status pgemm_kernel_attrs(pgemm_dtype dtype, const pgemm_config *cfg, int *smem_bytes,
+                                int *regs_per_thread, int *threads_per_block, int *blocks_per_sm) {
+    if (!cfg) return PGEMM_ERR_INVALID_VALUE;
+    pgemm_config c = *cfg;
+    if (c.bm == 0) c.bm = 128;
+    const KernelInfo *k = find_kernel(dtype, c);
+    if (!k) return PGEMM_ERR_UNSUPPORTED_CONFIG;
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    DeviceState *d = nullptr;
+    pgemm_status st = device_setup(&dev, &d);
+    if (st != PGEMM_OK) return st;
+    int bps = 0;
+    st = kernel_setup(*d, *k, &bps);
+    if (st != PGEMM_OK) return st;
+    cudaFuncAttributes fa{};
+    if (cudaFuncGetAttributes(&fa, k->func) != cudaSuccess) return PGEMM_ERR_CUDA;
+    if (smem_bytes) *smem_bytes = k->smem_bytes;
+    if (regs_per_thread) *regs_per_thread = fa.numRegs;
+    if (threads_per_block) *threads_per_block = k->threads;
+    if (blocks_per_sm) *blocks_per_sm = bps;
+    return PGEMM_OK;
+}
+
+pgemm_status pgemm_get_device_status(pgemm_stream_t stream) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    DeviceState *d = nullptr;
+    pgemm_status st = device_setup(&dev, &d);
+    if (st != PGEMM_OK) return st;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return PGEMM_ERR_CUDA;
+    uint32_t v = 0;
+    if (cudaMemcpy(&v, d->status, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return PGEMM_ERR_CUDA;
+    if (v == 0) return PGEMM_OK;
+    const uint32_t zero = 0;
+    if (cudaMemcpy(d->status, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+        return PGEMM_ERR_CUDA;
+    return (v & 0xF0000000u) == kStatusTimeout ? PGEMM_ERR_TIMEOUT : PGEMM_ERR_CUDA;
+}
+
+pgemm_status pgemm_selftest_wait_timeout(int limit_us, pgemm_stream_t stream) {
+    if (limit_us <= 0 || limit_us > 5000000) return PGEMM_ERR_INVALID_VALUE;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        int dev = 0;
+        DeviceState *d = nullptr;
+        pgemm_status st = device_setup(&dev, &d);
+        if (st != PGEMM_OK) return st;
+        KernelCtx ctx{d->status, static_cast<uint64_t>(limit_us) * 1000ull};
+        selftest_wait_kernel<<<1, 32, 0, stream>>>(ctx);
+        if (cudaGetLastError() != cudaSuccess) return PGEMM_ERR_CUDA;
+    }
+    return pgemm_get_device_status(stream);
+}
+
+const char *pgemm_status_string(pgemm_status status) {
+    switch (status) {
+        case PGEMM_OK: return "ok";
+        case PGEMM_ERR_INVALID_VALUE: return "invalid value";
+        case PGEMM_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+        case PGEMM_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs sm_103)";
+        case PGEMM_ERR_CUDA: return "CUDA error";
+        case PGEMM_ERR_TIMEOUT: return "device wait timed out";
+        case PGEMM_ERR_UNSUPPORTED_CONFIG: return "configuration not built";
+    }
+    return "unknown status";
+}
+
+int pgemm_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,28 @@
+// bf16 GEMM: C (fp32) = alpha * A (bf16) * B (bf16) + beta * C, products
+// accumulated in fp32 in tensor memory by tcgen05.mma kind::f16.  The kernel
+// body, its pipeline and its shared-memory layouts are in tc_gemm.cuh.
+#include "tc_gemm.cuh"
+
+namespace pg {
+
+template <int BN, int STAGES>
+using Bf16Cfg = TcCfg<BN, STAGES, /*KC=*/0, /*BF16=*/1, /*INT_FOLD=*/false>;
+
+template <int BN, int STAGES>
+static KernelInfo info_bf16() {
+    KernelInfo k = tc_info<Bf16Cfg<BN, STAGES>>();
+    k.launch_bf16 = launch_tc<Bf16Cfg<BN, STAGES>, LaunchBf16>;
+    return k;
+}
+
+const KernelInfo *bf16_kernels(int *count) {
+    static const KernelInfo table[] = {
+        info_bf16<256, 2>(), info_bf16<256, 3>(), info_bf16<256, 4>(),
+        info_bf16<128, 2>(), info_bf16<128, 3>(), info_bf16<128, 4>(),
+        info_bf16<128, 5>(), info_bf16<128, 6>(),
+    };
+    *count = static_cast<int>(sizeof(table) / sizeof(table[0]));
+    return table;
+}
+
+}  // namespace pg

@@ -1,0 +1,276 @@
+// fp32 GEMM with FFMA register tiles, fed by an S-stage TMA ring.
+//
+// This is the computation of the double-buffered SGEMM in "Double Buffering:
+// Software Pipelining the K-Loop" (section "The Kernel": a block tile, warp
+// tiles, per-thread register tiles of outer products, an alpha/beta epilogue)
+// with its two-buffer cp.async / register-transpose K-loop replaced by the
+// GB300 mechanism: K-tiles are streamed into S shared-memory slots with TMA
+// bulk-tensor copies that complete on the slot's "full" mbarrier, and the
+// consumer warps hand a slot back by arriving on its "empty" mbarrier
+// ("Software pipelines and asynchronous copies", section "Producer-consumer
+// synchronization").  No block-wide barrier remains in the steady state.
+//
+// The producer is lane 0 of warp 0, not a warp of its own: a fifth warp would
+// put 10 warps on an SM running two blocks, and the register file would then
+// allow only 168 registers a thread, too few for the 8 x 16 register tile.
+// Lane 0 issues the prologue (tiles 0 .. min(S, T) - 1, never beyond K) and
+// then, at the top of each K iteration, refills every slot whose "empty"
+// phase has completed (a non-blocking test), keeping up to S tiles in flight;
+// it blocks on "empty" only when the tile it is about to consume has not been
+// issued yet.
+//
+// Tile: BM x BN = 128 x 128, BK = 32 floats.  Four consumer warps in a 2 x 2
+// grid of 64 x 64 warp tiles; a warp's 32 lanes form 8 (m) x 4 (n) threads
+// with an 8 x 16 register tile each.  Thread rows are m = 8*i + tr (i = 0..7)
+// so the 8 rows a quarter-warp reads have distinct (m mod 8) and hit distinct
+// 16-byte chunks of the 128-byte swizzle; thread columns are four float4
+// groups n = 16*g + 4*tc.
+//
+// Shared-memory layouts (TMA-written):
+//   A slot: 128 rows (m) x 32 floats (k), 128-byte swizzled: element (m, k)
+//           at m*128 + (((k/4) ^ (m%8)) * 16) + (k%4)*4 bytes.  A thread reads
+//           float4 along k for each of its rows (no transpose is needed, unlike
+//           the page's k-major copy of A, which TMA cannot produce).
+//   B slot: 32 rows (k) x 128 floats (n), unswizzled rows of 512 bytes; a
+//           quarter-warp reads 4 consecutive float4 of one row.
+//
+// The products run as fma.rn.f32x2 (two fp32 FMAs per instruction, each
+// rounded exactly like a scalar FFMA), which halves the issue slots the
+// arithmetic takes so loads and address arithmetic fit beside it.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace pg {
+
+template <int STAGES>
+struct F32Cfg {
+    static constexpr int BM = 128, BN = 128, BK = 32;
+    static constexpr int A_BYTES = BM * BK * 4;  // 16 KB
+    static constexpr int B_BYTES = BK * BN * 4;  // 16 KB
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int CONSUMER_WARPS = 4;
+    static constexpr int THREADS = CONSUMER_WARPS * 32;
+    static constexpr int BAR_OFFSET = STAGES * STAGE_BYTES;
+    static constexpr int USED = BAR_OFFSET + 2 * STAGES * 8;
+    static constexpr int SMEM_BYTES = USED + 1024;
+    static_assert(SMEM_BYTES <= 232448, "shared memory");
+};
+
+__device__ __forceinline__ float4 lds128(uint32_t saddr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(saddr));
+    return v;
+}
+
+template <int STAGES>
+__global__ void __launch_bounds__(128, 2)
+    gemm_f32_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                    const __grid_constant__ CUtensorMap tmap_b,
+                    const GemmArgs<float, float> args, const KernelCtx ctx) {
+    using Cfg = F32Cfg<STAGES>;
+    constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align_1024(smem_raw);
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + STAGES * Cfg::A_BYTES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + Cfg::BAR_OFFSET);
+    uint64_t *empty = full + STAGES;
+
+    const uint32_t warp = warp_id_uniform();
+    const uint32_t lane = lane_id();
+
+    if (threadIdx.x == 0) {
+        prefetch_tmap(&tmap_a);
+        prefetch_tmap(&tmap_b);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], Cfg::CONSUMER_WARPS);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    int m0, n0;
+    tile_origin(blockIdx.x, args.num_m_tiles, args.num_n_tiles, args.group_m, BM, BN, m0, n0);
+    const int T = args.num_k_tiles;
+    const bool producer = threadIdx.x == 0;
+
+    // Issue the TMA copies of K-tile t into slot t % S.
+    auto issue = [&](int t) {
+        const int s = t % STAGES;
+        mbar_arrive_expect_tx(&full[s], Cfg::STAGE_BYTES);
+        tma_load_2d(sA + s * Cfg::A_BYTES, &tmap_a, &full[s], t * BK, m0);
+        tma_load_2d(sB + s * Cfg::B_BYTES, &tmap_b, &full[s], n0, t * BK);
+    };
+    int next_load = 0;  // tiles [0, next_load) have been issued (producer lane only)
+    if (producer) {
+        // prologue: fill min(S, T) slots
+        for (; next_load < T && next_load < STAGES; ++next_load) issue(next_load);
+    }
+
+    // ---------------- consumers ----------------
+    const int wm = static_cast<int>(warp) >> 1;  // warp tile row (0..1)
+    const int wn = static_cast<int>(warp) & 1;   // warp tile column (0..1)
+    const int tr = static_cast<int>(lane) >> 2;  // 0..7
+    const int tc = static_cast<int>(lane) & 3;   // 0..3
+
+    // acc[i][2*g + h] holds columns 16*g + 4*tc + 2*h + {0,1} of row 8*i + tr
+    float2 acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = make_float2(0.f, 0.f);
+
+    // byte offsets inside a slot
+    const uint32_t a_row0 = static_cast<uint32_t>((wm * 64 + tr) * 128);  // row 8*i+tr: + i*1024
+    const uint32_t b_col0 = static_cast<uint32_t>((wn * 64 + tc * 4) * 4);
+
+    bool ok = true;
+    for (int kt = 0; kt < T; ++kt) {
+        if (producer) {
+            // steady state: refill released slots, up to S tiles ahead of kt
+            while (next_load < T && next_load < kt + STAGES) {
+                const int prev = next_load - STAGES;  // last tile that used this slot
+                uint64_t *e = &empty[next_load % STAGES];
+                const uint32_t par = static_cast<uint32_t>(prev / STAGES) & 1u;
+                if (!mbar_test_wait(e, par)) {
+                    if (next_load > kt) break;  // not needed yet: try again next iteration
+                    if (!mbar_wait(e, par, ctx, kSiteProducerEmpty)) break;
+                }
+                issue(next_load++);
+            }
+        }
+        const uint32_t s = kt % STAGES, ph = (kt / STAGES) & 1u;
+        if (!mbar_wait(&full[s], ph, ctx, kSiteConsumerFull)) {
+            ok = false;
+            break;
+        }
+        const uint32_t a_base = smem_u32(sA + s * Cfg::A_BYTES) + a_row0;
+        const uint32_t b_base = smem_u32(sB + s * Cfg::B_BYTES) + b_col0;
+#pragma unroll 2
+        for (int k4 = 0; k4 < BK / 4; ++k4) {
+            float4 a[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)  // (m % 8) == tr for every row of this thread
+                a[i] = lds128(a_base + i * 1024 + ((k4 ^ tr) << 4));
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                float4 b[4];
+                const uint32_t brow = b_base + (k4 * 4 + kk) * (BN * 4);
+#pragma unroll
+                for (int g = 0; g < 4; ++g) b[g] = lds128(brow + g * 64);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
+                    const float2 a2 = make_float2(av, av);
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        acc[i][2 * g] = __ffma2_rn(a2, make_float2(b[g].x, b[g].y), acc[i][2 * g]);
+                        acc[i][2 * g + 1] =
+                            __ffma2_rn(a2, make_float2(b[g].z, b[g].w), acc[i][2 * g + 1]);
+                    }
+                }
+            }
+        }
+        // Release the slot: this warp's reads of it are done.
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    if (!ok) return;
+
+    // ---------------- epilogue: alpha * acc + beta * C ----------------
+    const bool read_c = args.beta != 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int row = m0 + wm * 64 + 8 * i + tr;
+        if (row >= args.M) continue;
+        float *crow = args.C + static_cast<long long>(row) * args.ldc;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const int col = n0 + wn * 64 + 16 * g + 4 * tc;
+            float *cp = crow + col;
+            const float v[4] = {acc[i][2 * g].x, acc[i][2 * g].y, acc[i][2 * g + 1].x,
+                                acc[i][2 * g + 1].y};
+            if (col + 4 <= args.N && (reinterpret_cast<uintptr_t>(cp) & 15u) == 0) {
+                float4 o;
+                if (read_c) {
+                    const float4 c = *reinterpret_cast<const float4 *>(cp);
+                    o = make_float4(axpby(args.alpha, v[0], args.beta, c.x),
+                                    axpby(args.alpha, v[1], args.beta, c.y),
+                                    axpby(args.alpha, v[2], args.beta, c.z),
+                                    axpby(args.alpha, v[3], args.beta, c.w));
+                } else {
+                    o = make_float4(args.alpha * v[0], args.alpha * v[1], args.alpha * v[2],
+                                    args.alpha * v[3]);
+                }
+                *reinterpret_cast<float4 *>(cp) = o;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (col + e < args.N)
+                        cp[e] = read_c ? axpby(args.alpha, v[e], args.beta, cp[e])
+                                       : args.alpha * v[e];
+            }
+        }
+    }
+}
+
+// ----------------------------------------------------------------- host ---
+template <int STAGES>
+static cudaError_t launch_f32_impl(const LaunchF32 &p, cudaStream_t stream) {
+    using Cfg = F32Cfg<STAGES>;
+    GemmArgs<float, float> a{};
+    a.M = p.M;
+    a.N = p.N;
+    a.K = p.K;
+    a.num_m_tiles = (p.M + Cfg::BM - 1) / Cfg::BM;
+    a.num_n_tiles = (p.N + Cfg::BN - 1) / Cfg::BN;
+    a.num_k_tiles = (p.K + Cfg::BK - 1) / Cfg::BK;
+    a.group_m = p.group_m > 0 ? p.group_m : 8;
+    a.alpha = p.alpha;
+    a.beta = p.beta;
+    a.C = p.C;
+    a.ldc = p.ldc;
+    const int tiles = a.num_m_tiles * a.num_n_tiles;
+    if (tiles < 1) return cudaSuccess;
+    gemm_f32_kernel<STAGES><<<tiles, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(*p.tmap_a, *p.tmap_b,
+                                                                             a, p.ctx);
+    return cudaGetLastError();
+}
+
+template <int STAGES>
+static KernelInfo info_f32() {
+    using Cfg = F32Cfg<STAGES>;
+    KernelInfo k;
+    k.bm = Cfg::BM;
+    k.bn = Cfg::BN;
+    k.bk = Cfg::BK;
+    k.stages = STAGES;
+    k.threads = Cfg::THREADS;
+    k.smem_bytes = Cfg::SMEM_BYTES;
+    k.a_box_x = Cfg::BK;   // 32 floats = 128 bytes, swizzled
+    k.a_box_y = Cfg::BM;
+    k.b_box_x = Cfg::BN;   // 128 floats = 512 bytes, unswizzled
+    k.b_box_y = Cfg::BK;
+    k.a_swizzle128 = true;
+    k.b_swizzle128 = false;
+    k.func = reinterpret_cast<const void *>(gemm_f32_kernel<STAGES>);
+    k.launch_f32 = launch_f32_impl<STAGES>;
+    return k;
+}
+
+const KernelInfo *f32_kernels(int *count) {
+    static const KernelInfo table[] = {info_f32<2>(), info_f32<3>(), info_f32<4>(), info_f32<5>(),
+                                       info_f32<6>()};
+    *count = static_cast<int>(sizeof(table) / sizeof(table[0]));
+    return table;
+}
+
+}  // namespace pg

@@ -1,0 +1,73 @@
+// Host-side interface between the dispatch layer (api.cu) and the kernel
+// translation units: one KernelInfo per compiled (tile, stages) instance.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ptx.cuh"
+
+namespace pg {
+
+// Shared memory per SM on sm_100-family GPUs and the per-block reservation.
+constexpr int kSmemPerSm = 233472;
+constexpr int kSmemReservedPerBlock = 1024;
+
+// Dynamic shared memory to request so that (a) `used` bytes fit and (b) no
+// more than `max_blocks` blocks can be resident on one SM.
+constexpr int smem_request(int used, int max_blocks) {
+    const int cap = kSmemPerSm / (max_blocks + 1) - kSmemReservedPerBlock + 1;
+    return used > cap ? used : cap;
+}
+
+struct LaunchCommon {
+    int M, N, K;
+    long long ldc;
+    int group_m;        // raster group (0 = kernel default)
+    int sm_count;
+    int blocks_per_sm;  // resident blocks per SM for this kernel (occupancy query)
+    const CUtensorMap *tmap_a;
+    const CUtensorMap *tmap_b;
+    KernelCtx ctx;
+};
+
+struct LaunchBf16 : LaunchCommon {
+    float alpha, beta;
+    float *C;
+};
+
+struct LaunchF32 : LaunchCommon {
+    float alpha, beta;
+    float *C;
+};
+
+struct LaunchI8 : LaunchCommon {
+    int32_t alpha, beta;
+    int32_t *C;
+};
+
+struct KernelInfo {
+    int bm = 0, bn = 0, bk = 0, stages = 0;
+    int threads = 0;
+    int smem_bytes = 0;
+    // Operand boxes the tensor maps must be encoded with (elements, x = innermost).
+    int a_box_x = 0, a_box_y = 0, b_box_x = 0, b_box_y = 0;
+    bool a_swizzle128 = true, b_swizzle128 = true;
+    const void *func = nullptr;
+    cudaError_t (*launch_bf16)(const LaunchBf16 &, cudaStream_t) = nullptr;
+    cudaError_t (*launch_f32)(const LaunchF32 &, cudaStream_t) = nullptr;
+    cudaError_t (*launch_i8)(const LaunchI8 &, cudaStream_t) = nullptr;
+};
+
+const KernelInfo *bf16_kernels(int *count);
+const KernelInfo *f32_kernels(int *count);
+const KernelInfo *i8_kernels(int *count);
+
+}  // namespace pg
+
+namespace pg {
+// int8 -> fp16 widening pass (gemm_i8.cu): dst rows of pitch dld elements.
+cudaError_t launch_widen_i8(const int8_t *src, long long sld, void *dst, long long dld, int rows,
+                            int cols, int sm_count, cudaStream_t stream);
+}  // namespace pg

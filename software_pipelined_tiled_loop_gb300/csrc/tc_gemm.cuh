@@ -1,0 +1,318 @@
+// Tensor-core GEMM kernel body shared by the bf16 and the exact-int8 paths:
+// 16-bit operands (bf16, or fp16 holding widened int8), fp32 accumulators in
+// tensor memory (tcgen05), fed by an S-stage TMA ring.
+//
+// The K-loop is the software pipeline of "Double Buffering: Software
+// Pipelining the K-Loop" (sections "Two Stages, One Barrier" and "Mechanics")
+// generalised to S stages and split across warps the way "Software pipelines
+// and asynchronous copies" describes the state machine (sections "Prologue,
+// steady state, and epilogue" and "Producer-consumer synchronization"):
+//
+//   warp 0 (one lane)  producer: for every K-tile t, wait empty[t % S], post
+//                      the stage's byte count on full[t % S] and issue the TMA
+//                      copies of the A and B panels.  The first S waits pass at
+//                      once: that is the prologue, and it issues min(S, T)
+//                      loads, never one beyond K.
+//   warp 1 (one lane)  MMA issuer: wait full[t % S], issue BK/16 tcgen05.mma
+//                      into a TMEM accumulator, then tcgen05.commit to
+//                      empty[t % S] so the stage is refilled only after the
+//                      tensor core has finished reading it (the reuse edge).
+//                      After the last K-tile of an accumulation round it
+//                      commits to acc_full (the drain).  Warp 1 owns TMEM.
+//   warps 2..5         epilogue: wait acc_full, tcgen05.ld the accumulator
+//                      (each warp reads its own 32-lane TMEM quadrant), then
+//                      release acc_empty.
+//
+// An accumulation round is the whole K range of an output tile (bf16), or a
+// chunk of KC K-tiles (exact int8: a chunk's fp32 partial sums of fp16
+// products of int8 values stay integers below 2^24 and are exact; the
+// epilogue converts each chunk to int32 and adds it into registers).
+//
+// The kernel is persistent (grid = resident blocks, output tiles strided by
+// the grid) and TMEM holds two accumulators, so the epilogue of one round
+// overlaps the main loop of the next.  Stage index t % S and phase parity
+// (t / S) & 1 come from a running counter, valid for any S (the page's XOR
+// swap is valid for two stages only).
+//
+// Shared-memory layouts (both 128-byte swizzled, written by TMA):
+//   A stage: BM = 128 rows (m) x 64 elements (k) -> K-major operand: rows of
+//            128 B, 8-row groups 1024 B apart (SBO = 1024); K = 16 -> +32 B.
+//   B stage: BN/64 boxes of 64 (n) x 64 (k) -> N-major operand: each box is
+//            64 k-rows of 128 B, 8-k-row groups 1024 B apart (SBO = 1024),
+//            boxes (64-column n blocks) BK*128 B apart (LBO); K = 16 -> +2048 B.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <type_traits>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace pg {
+
+// BN: tile width; STAGES: ring depth; KC: K-tiles per accumulation round (0 =
+// all of K); BF16: operand type (1 = bf16, 0 = fp16); INT_FOLD: exact-int8
+// epilogue (fold fp32 chunk sums into int32 registers).
+template <int BN_, int STAGES_, int KC_, int BF16_, bool INT_FOLD_>
+struct TcCfg {
+    static constexpr int BM = 128, BN = BN_, BK = 64, STAGES = STAGES_, KC = KC_;
+    static constexpr int BF16 = BF16_;
+    static constexpr bool INT_FOLD = INT_FOLD_;
+    using Scalar = typename std::conditional<INT_FOLD, int32_t, float>::type;
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int ACC_COLS = BN;        // fp32 accumulator: one TMEM column per n
+    static constexpr int TMEM_COLS = 2 * BN;   // two accumulators
+    static constexpr int THREADS = 192;
+    static constexpr int BAR_OFFSET = STAGES * STAGE_BYTES;
+    static constexpr int NUM_BARS = 2 * STAGES + 5;
+    static constexpr int USED = BAR_OFFSET + NUM_BARS * 8 + 16;
+    // TMEM has 512 columns per SM: at most 512 / TMEM_COLS blocks may share an
+    // SM, or a block would stall in tcgen05.alloc.  The shared-memory request
+    // is padded so that occupancy never exceeds that.
+    static constexpr int MAX_BLOCKS = 512 / TMEM_COLS;
+    static constexpr int SMEM_BYTES = smem_request(USED + 1024, MAX_BLOCKS);
+    static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
+    static_assert(!INT_FOLD || BN == 128, "the int32 fold keeps one 128-column row per thread");
+    static_assert(USED + 1024 <= 232448, "shared memory");
+};
+
+template <class Cfg>
+__global__ void __launch_bounds__(192, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                   const __grid_constant__ CUtensorMap tmap_b,
+                   const GemmArgs<typename Cfg::Scalar, typename Cfg::Scalar> args,
+                   const KernelCtx ctx) {
+    constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align_1024(smem_raw);
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + STAGES * Cfg::A_BYTES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + Cfg::BAR_OFFSET);
+    uint64_t *empty = full + STAGES;
+    uint64_t *acc_full = empty + STAGES;  // [2]
+    uint64_t *acc_empty = acc_full + 2;   // [2]
+    uint64_t *mma_done = acc_empty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+
+    const uint32_t warp = warp_id_uniform();
+    const uint32_t lane = lane_id();
+
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmap_a);
+        prefetch_tmap(&tmap_b);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 4);
+        }
+        mbar_init(mma_done, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int num_tiles = args.num_m_tiles * args.num_n_tiles;
+    const int T = args.num_k_tiles;
+    // accumulation rounds per output tile
+    const int KCt = Cfg::KC > 0 ? Cfg::KC : (T > 0 ? T : 1);
+    const int rounds = T > 0 ? (T + KCt - 1) / KCt : 0;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- producer: TMA into the stage ring ----------------
+            uint32_t it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                int m0, n0;
+                tile_origin(tile, args.num_m_tiles, args.num_n_tiles, args.group_m, BM, BN, m0, n0);
+                for (int kt = 0; kt < T; ++kt, ++it) {
+                    const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+                    if (!mbar_wait(&empty[s], ph ^ 1u, ctx, kSiteProducerEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[s], Cfg::STAGE_BYTES);
+                    tma_load_2d(sA + s * Cfg::A_BYTES, &tmap_a, &full[s], kt * BK, m0);
+#pragma unroll
+                    for (int j = 0; j < BN / 64; ++j)
+                        tma_load_2d(sB + s * Cfg::B_BYTES + j * (BK * 128), &tmap_b, &full[s],
+                                    n0 + j * 64, kt * BK);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer ----------------
+            constexpr uint32_t idesc = idesc_f16(BM, BN, Cfg::BF16, /*A K-major*/ 0,
+                                                 /*B N-major*/ 1);
+            uint32_t it = 0, gr = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                for (int r = 0; ok && r < rounds; ++r, ++gr) {
+                    const uint32_t ab = gr & 1u, aph = (gr >> 1) & 1u;
+                    if (!mbar_wait(&acc_empty[ab], aph ^ 1u, ctx, kSiteMmaAccEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + ab * Cfg::ACC_COLS;
+                    const int k_end = min(T, (r + 1) * KCt);
+                    for (int kt = r * KCt; kt < k_end; ++kt, ++it) {
+                        const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+                        if (!mbar_wait(&full[s], ph, ctx, kSiteMmaFull)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t a_addr = smem_u32(sA + s * Cfg::A_BYTES);
+                        const uint32_t b_addr = smem_u32(sB + s * Cfg::B_BYTES);
+                        const bool first = kt == r * KCt;
+#pragma unroll
+                        for (int k = 0; k < BK / 16; ++k) {
+                            const uint64_t ad = smem_desc_sw128(a_addr + k * 32, 16, 1024);
+                            const uint64_t bd = smem_desc_sw128(b_addr + k * 2048, BK * 128, 1024);
+                            umma_f16_ss(d_tmem, ad, bd, idesc, (first && k == 0) ? 0u : 1u);
+                        }
+                        umma_commit(&empty[s]);  // stage s is free once these MMAs read it
+                    }
+                    if (ok) umma_commit(&acc_full[ab]);  // round complete -> epilogue
+                }
+            }
+            umma_commit(mma_done);
+            mbar_wait(mma_done, 0, ctx, kSiteMmaDone);
+        }
+    } else {
+        // ---------------- epilogue warps 2..5 ----------------
+        const uint32_t q = warp & 3u;  // the TMEM lane quadrant this warp may read
+        uint32_t gr = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            int m0, n0;
+            tile_origin(tile, args.num_m_tiles, args.num_n_tiles, args.group_m, BM, BN, m0, n0);
+            const int row = m0 + static_cast<int>(q * 32 + lane);
+            if constexpr (Cfg::INT_FOLD) {
+                // exact int8: sum the chunks' integer-valued fp32 partials in int32
+                uint32_t acc[BN];
+#pragma unroll
+                for (int j = 0; j < BN; ++j) acc[j] = 0u;
+                for (int r = 0; r < rounds; ++r, ++gr) {
+                    const uint32_t ab = gr & 1u, aph = (gr >> 1) & 1u;
+                    if (!mbar_wait(&acc_full[ab], aph, ctx, kSiteEpilogueFull)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t t_row = tmem_base + ((q * 32u) << 16) + ab * Cfg::ACC_COLS;
+#pragma unroll
+                    for (int c = 0; c < BN; c += 32) {
+                        uint32_t v[32];
+                        tmem_ld_32x32b_x32(t_row + c, v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            acc[c + e] += static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[e])));
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&acc_empty[ab]);
+                }
+                if (!ok) break;
+#pragma unroll
+                for (int c = 0; c < BN; c += 32) store_row32(args, row, n0 + c, acc + c, true);
+            } else {
+                if (rounds > 0) {
+                    const uint32_t ab = gr & 1u, aph = (gr >> 1) & 1u;
+                    if (!mbar_wait(&acc_full[ab], aph, ctx, kSiteEpilogueFull)) break;
+                    tc_fence_after();
+                    const uint32_t t_row = tmem_base + ((q * 32u) << 16) + ab * Cfg::ACC_COLS;
+#pragma unroll 1
+                    for (int c = 0; c < BN; c += 32) {
+                        uint32_t v[32];
+                        tmem_ld_32x32b_x32(t_row + c, v);
+                        tmem_ld_wait();
+                        store_row32(args, row, n0 + c, v, true);
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&acc_empty[ab]);
+                    ++gr;
+                } else {
+                    // K == 0: C = beta * C, tensor memory is never read
+                    uint32_t zero[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) zero[e] = 0u;
+#pragma unroll 1
+                    for (int c = 0; c < BN; c += 32) store_row32(args, row, n0 + c, zero, false);
+                }
+            }
+        }
+    }
+
+    // ---------------- teardown ----------------
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+// ----------------------------------------------------------------- host ---
+template <class Cfg, class P>
+static cudaError_t launch_tc(const P &p, cudaStream_t stream) {
+    GemmArgs<typename Cfg::Scalar, typename Cfg::Scalar> a{};
+    a.M = p.M;
+    a.N = p.N;
+    a.K = p.K;
+    a.num_m_tiles = (p.M + Cfg::BM - 1) / Cfg::BM;
+    a.num_n_tiles = (p.N + Cfg::BN - 1) / Cfg::BN;
+    a.num_k_tiles = (p.K + Cfg::BK - 1) / Cfg::BK;
+    a.group_m = p.group_m > 0 ? p.group_m : 16;
+    a.alpha = p.alpha;
+    a.beta = p.beta;
+    a.C = p.C;
+    a.ldc = p.ldc;
+    const int tiles = a.num_m_tiles * a.num_n_tiles;
+    const int per_sm = p.blocks_per_sm < Cfg::MAX_BLOCKS ? p.blocks_per_sm : Cfg::MAX_BLOCKS;
+    int grid = p.sm_count * (per_sm > 0 ? per_sm : 1);
+    if (grid > tiles) grid = tiles;
+    if (grid < 1) return cudaSuccess;
+    tc_gemm_kernel<Cfg><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(*p.tmap_a, *p.tmap_b, a,
+                                                                         p.ctx);
+    return cudaGetLastError();
+}
+
+template <class Cfg>
+static KernelInfo tc_info() {
+    KernelInfo k;
+    k.bm = Cfg::BM;
+    k.bn = Cfg::BN;
+    k.bk = Cfg::BK;
+    k.stages = Cfg::STAGES;
+    k.threads = Cfg::THREADS;
+    k.smem_bytes = Cfg::SMEM_BYTES;
+    k.a_box_x = Cfg::BK;
+    k.a_box_y = Cfg::BM;
+    k.b_box_x = 64;
+    k.b_box_y = Cfg::BK;
+    k.a_swizzle128 = k.b_swizzle128 = true;
+    k.func = reinterpret_cast<const void *>(tc_gemm_kernel<Cfg>);
+    return k;
+}
+
+}  // namespace pg
