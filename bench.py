@@ -129,7 +129,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
@@ -182,7 +182,8 @@ def _to_dev(torch, x):
     return torch.from_numpy(np.ascontiguousarray(x)).cuda()
 
 
-def run_gpu_workload(name: str, steps: int, warmup: int, dist_ctx, with_e2e: bool) -> dict:
+def run_gpu_workload(name: str, steps: int, warmup: int, dist_ctx, with_e2e: bool,
+                     clocks: "ClockSampler | None" = None) -> dict:
     import torch
 
     import software_pipelined_tiled_loop_gb300 as pg
@@ -205,6 +206,9 @@ def run_gpu_workload(name: str, steps: int, warmup: int, dist_ctx, with_e2e: boo
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     dist_ctx.barrier()
     torch.cuda.synchronize()
+    if clocks is not None:
+        clocks.start()
+    t_wall = time.perf_counter()
     for i in range(steps):
         flush.fill_(float(i))  # evict A, B, C from L2 between timed steps
         starts[i].record(stream)
@@ -213,6 +217,18 @@ def run_gpu_workload(name: str, steps: int, warmup: int, dist_ctx, with_e2e: boo
     torch.cuda.synchronize()
     dist_ctx.barrier()
     per_step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    clk = None
+    if clocks is not None:
+        # nvidia-smi samples every 100 ms: if the timed region was shorter than
+        # one second, the same steps keep running (untimed) until the clock
+        # window covers a second of this load
+        while time.perf_counter() - t_wall < 1.0:
+            for i in range(8):
+                flush.fill_(float(i))
+                fn(M, N, K, alpha, dA, dB, beta, dC)
+            torch.cuda.synchronize()
+        clk = clocks.stop()
+        clk["window_s"] = round(time.perf_counter() - t_wall, 2)
     if pg.pgemm_get_device_status() != 0:
         raise RuntimeError("device status after timed steps")
     total_ms = dist_ctx.max(sum(per_step_ms))
@@ -222,7 +238,7 @@ def run_gpu_workload(name: str, steps: int, warmup: int, dist_ctx, with_e2e: boo
            "tflops": flops * steps * dist_ctx.world / (total_ms * 1e-3) / 1e12,
            "per_gpu_tflops": flops * steps / (total_ms * 1e-3) / 1e12,
            "launches_per_step": 1 if dtype != "i8" else 3,
-           "config": pg.pgemm_default_config(dtype, M, N, K)}
+           "config": pg.pgemm_default_config(dtype, M, N, K), "clocks": clk}
 
     if with_e2e:
         # end to end through the public call: pinned host -> device, GEMM, C -> host
@@ -290,6 +306,65 @@ def oracle_sample(name: str, target_s: float) -> dict:
             "seconds": round(dt2, 2)}
 
 
+# ------------------------------------------------------------------ sweep ---
+SWEEP_SHAPES = {
+    # dtype -> list of (M, N, K, recipe); the bf16 K list is the K-sweep workload
+    "f32": [(4096, 4096, 4096, "f32_uniform_beta")],
+    "i8": [(4096, 4096, 4096, "i8_uniform")],
+    "bf16": [(8192, 8192, 8192, "bf16_normal")] +
+            [(4096, 4096, k, "bf16_normal") for k in (32, 64, 128, 512, 2048, 16384)] +
+            [(4095, 4097, 4100, "bf16_normal")],
+}
+
+
+def run_point(dtype, M, N, K, recipe, cfg, steps, warmup, seed=None):
+    """Time one (shape, configuration) point; returns a dict (no correctness check:
+    the parity tests cover every configuration)."""
+    import torch
+
+    import software_pipelined_tiled_loop_gb300 as pg
+
+    seed = si.config_seed(5, K % 251) if seed is None else seed
+    A, B, C0, alpha, beta, _ = si.workload(recipe, M, N, K, seed)
+    fn = {"f32": pg.gemm_f32_ex, "bf16": pg.gemm_bf16_ex, "i8": pg.gemm_i8_ex}[dtype]
+    dA, dB, dC = _to_dev(torch, A), _to_dev(torch, B), _to_dev(torch, C0)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        fn(M, N, K, alpha, dA, dB, beta, dC, config=cfg)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for i in range(steps):  # queued back to back: host work overlaps the GPU
+        flush.fill_(float(i))
+        ev[i][0].record(stream)
+        fn(M, N, K, alpha, dA, dB, beta, dC, config=cfg)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in ev]
+    status = pg.pgemm_get_device_status()
+    attrs = pg.pgemm_kernel_attrs(dtype, cfg)
+    med = statistics.median(ms)
+    flops = 2.0 * M * N * K
+    out_bytes = M * N * 4 * (2 if beta != 0 else 1)
+    in_bytes = (M * K + K * N) * {"f32": 4, "bf16": 2, "i8": 1}[dtype]
+    del dA, dB, dC, flush
+    return {"dtype": dtype, "M": M, "N": N, "K": K, "bm": cfg[0], "bn": cfg[1], "bk": cfg[2],
+            "stages": cfg[3], "k_tiles": -(-K // cfg[2]), **attrs, "ms_median": round(med, 4),
+            "ms_min": round(min(ms), 4), "tflops": round(flops / (med * 1e-3) / 1e12, 2),
+            "gbs": round((in_bytes + out_bytes) / (med * 1e-3) / 1e9, 1), "status": status}
+
+
+def sweep(dtypes, steps, warmup, only_k=None):
+    import software_pipelined_tiled_loop_gb300 as pg
+    for dtype in dtypes:
+        for (M, N, K, recipe) in SWEEP_SHAPES[dtype]:
+            if only_k is not None and K not in only_k:
+                continue
+            for cfg in pg.pgemm_list_configs(dtype):
+                print(json.dumps(run_point(dtype, M, N, K, recipe, cfg, steps, warmup)), flush=True)
+
+
 # ------------------------------------------------------------ distributed ---
 class DistCtx:
     def __init__(self):
@@ -325,16 +400,37 @@ class DistCtx:
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["pgemm", "reference"], default="pgemm")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-also", action="store_true", help="skip the other workloads")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work of the oracle sample (cpu_baseline / reference arm)")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end timing")
+    ap.add_argument("--sweep", default=None,
+                    help="comma list of dtypes: time every built (tile, stages) config on the "
+                         "sweep shapes, one JSON line per point")
+    ap.add_argument("--sweep-k", default=None, help="comma list of K values to restrict the sweep")
+    ap.add_argument("--point", default=None,
+                    help="dtype,M,N,K,bm,bn,bk,stages: time one point (for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
+    if args.sweep or args.point:
+        from software_pipelined_tiled_loop_gb300 import build as pgbuild
+        pgbuild.build()
+        if args.sweep:
+            ks = {int(k) for k in args.sweep_k.split(",")} if args.sweep_k else None
+            sweep(args.sweep.split(","), args.steps, args.warmup, ks)
+        else:
+            f = args.point.split(",")
+            dt, (M, N, K, bm, bn, bk, st) = f[0], map(int, f[1:])
+            recipe = {"f32": "f32_uniform_beta", "bf16": "bf16_normal", "i8": "i8_uniform"}[dt]
+            print(json.dumps(run_point(dt, M, N, K, recipe, (bm, bn, bk, st), args.steps,
+                                       args.warmup)))
+        return
 
     dtype, M, N, K, recipe, seed = WORKLOADS[args.workload]
     config = {"workload": args.workload, "dtype": dtype, "M": M, "N": N, "K": K,
@@ -344,17 +440,19 @@ def main():
         rank = int(os.environ.get("RANK", "0"))
         if rank != 0:
             return
-        per = []
+        per, secs = [], []
         for _ in range(args.warmup):
-            pass  # the oracle has no warm-up state; each step is a full sample
+            oracle_sample(args.workload, 0.05)  # untimed: loads the library, touches the operands
         sample = None
         for _ in range(args.steps):
             sample = oracle_sample(args.workload, max(1.0, args.cpu_seconds / args.steps))
             per.append(sample["value"])
+            secs.append(sample["seconds"])
         value = statistics.median(per)
         line = {"metric": METRIC, "value": value, "unit": sample["unit"], "impl": "reference",
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-                "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+                "ms_per_step": round(1000 * statistics.median(secs), 1), "higher_is_better": True,
+                "scaling": "weak",
                 "vs_baseline": None, "dtype": {"f32": "f32", "bf16": "bf16", "i8": "int8"}[dtype],
                 "data": "synthetic", "config": config,
                 "cpu_baseline": {"value": value, "unit": sample["unit"], "cores": sample["cores"],
@@ -378,25 +476,25 @@ def main():
     gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(ctx.local_rank)).split(",")[0] or 0) \
         if os.environ.get("CUDA_VISIBLE_DEVICES", "").replace(",", "").isdigit() else ctx.local_rank
 
-    clocks = ClockSampler(gpu_index)
-    clocks.start()
-    main_res = run_gpu_workload(args.workload, args.steps, args.warmup, ctx, with_e2e=True)
-    clk = clocks.stop()
+    main_res = run_gpu_workload(args.workload, args.steps, args.warmup, ctx,
+                                with_e2e=not args.no_e2e, clocks=ClockSampler(gpu_index))
+    clk = main_res["clocks"]
 
     also = {}
     if not args.no_also:
         for other in WORKLOADS:
             if other == args.workload:
                 continue
-            r = run_gpu_workload(other, max(5, args.steps // 2), args.warmup, ctx, with_e2e=False)
-            also[other] = {"value": round(r["tflops"], 2),
+            r = run_gpu_workload(other, max(5, args.steps // 2), args.warmup, ctx, with_e2e=False,
+                                 clocks=ClockSampler(gpu_index))
+            also[other] = {"value": round(r["tflops"], 2), "clocks": r["clocks"],
                            "unit": "TOP/s" if r["dtype"] == "i8" else "TFLOP/s",
                            "ms_per_step": round(r["ms_per_step"], 4),
                            "roofline": roofline_for(r["dtype"], r["per_gpu_tflops"], sm_count, peaks),
                            "config": r["config"]}
 
     cpu = None
-    if ctx.rank == 0 and ctx.world == 1:
+    if ctx.rank == 0 and ctx.world == 1 and not args.no_cpu:
         cpu = oracle_sample(args.workload, args.cpu_seconds)
 
     if ctx.rank == 0:
@@ -418,7 +516,8 @@ def main():
             "e2e": main_res.get("e2e"),
             "gpu_launches": main_res["launches_per_step"] * args.steps,
             "clocks": {"sm_mhz": clk.get("sm_mhz"), "sm_max_mhz": clk.get("sm_max_mhz"),
-                       "reasons": clk.get("reasons")},
+                       "reasons": clk.get("reasons"), "samples": clk.get("samples"),
+                       "window_s": clk.get("window_s")},
             "also": also,
         }
         print(json.dumps(line))

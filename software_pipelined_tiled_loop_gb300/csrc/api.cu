@@ -90,6 +90,11 @@ static pgemm_status kernel_setup(DeviceState &d, const KernelInfo &k, int *block
         if (cudaFuncSetAttribute(k.func, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  k.smem_bytes) != cudaSuccess)
             return PGEMM_ERR_CUDA;
+        // all of the unified L1/shared storage as shared memory, so that the
+        // occupancy the shared-memory request was sized for is reachable
+        if (cudaFuncSetAttribute(k.func, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+            return PGEMM_ERR_CUDA;
         int n = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k.func, k.threads, k.smem_bytes) !=
             cudaSuccess)
@@ -129,7 +134,8 @@ static pgemm_config default_config(pgemm_dtype dt, int M, int N, int K, int sm_c
             c.stages = 4;
         }
     } else {
-        c.bn = 128;
+        const long long tiles256 = (long long)((M + 127) / 128) * ((N + 255) / 256);
+        c.bn = tiles256 >= sm_count ? 256 : 128;
         c.stages = 4;
     }
     return c;
@@ -288,27 +294,37 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
     }
     if (st != PGEMM_OK) return st;
 
+    // C as a tensor map (32 x 32 boxes, 128-byte swizzle) when its rows are
+    // 16-byte aligned, so that the tensor-core epilogue can store by TMA.
+    alignas(64) CUtensorMap tc_map;
+    const CUtensorMap *tmap_c = nullptr;
+    if (k->c_tma && aligned16(C) && (static_cast<long long>(N) * 4) % 16 == 0) {
+        const CUtensorMapDataType ct =
+            KIND == Kind::I8 ? CU_TENSOR_MAP_DATA_TYPE_INT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+        if (encode_2d(&tc_map, ct, 4, C, N, M, N, 32, 32, true) == PGEMM_OK) tmap_c = &tc_map;
+    }
+
     cudaError_t e = cudaSuccess;
     KernelCtx ctx{d->status, kDefaultWaitLimitNs};
     if constexpr (KIND == Kind::F32) {
         LaunchF32 p{};
         p.M = M; p.N = N; p.K = K; p.ldc = N; p.group_m = 0;
         p.sm_count = d->sm_count; p.blocks_per_sm = blocks_per_sm;
-        p.tmap_a = &ta; p.tmap_b = &tb; p.ctx = ctx;
+        p.tmap_a = &ta; p.tmap_b = &tb; p.tmap_c = tmap_c; p.ctx = ctx;
         p.alpha = alpha; p.beta = beta; p.C = C;
         e = k->launch_f32(p, stream);
     } else if constexpr (KIND == Kind::BF16) {
         LaunchBf16 p{};
         p.M = M; p.N = N; p.K = K; p.ldc = N; p.group_m = 0;
         p.sm_count = d->sm_count; p.blocks_per_sm = blocks_per_sm;
-        p.tmap_a = &ta; p.tmap_b = &tb; p.ctx = ctx;
+        p.tmap_a = &ta; p.tmap_b = &tb; p.tmap_c = tmap_c; p.ctx = ctx;
         p.alpha = alpha; p.beta = beta; p.C = C;
         e = k->launch_bf16(p, stream);
     } else {
         LaunchI8 p{};
         p.M = M; p.N = N; p.K = K; p.ldc = N; p.group_m = 0;
         p.sm_count = d->sm_count; p.blocks_per_sm = blocks_per_sm;
-        p.tmap_a = &ta; p.tmap_b = &tb; p.ctx = ctx;
+        p.tmap_a = &ta; p.tmap_b = &tb; p.tmap_c = tmap_c; p.ctx = ctx;
         p.alpha = alpha; p.beta = beta; p.C = C;
         e = k->launch_i8(p, stream);
     }

@@ -30,6 +30,7 @@ struct GemmArgs {
     Scalar alpha, beta;
     Out *C;           // row-major, leading dimension ldc
     long long ldc;
+    int c_tma;        // 1: C is also described by a tensor map (TMA stores allowed)
 };
 
 // Output tile `tile` -> (m0, n0).  Tiles are visited in groups of `group_m`

@@ -5,8 +5,11 @@
 
 namespace pg {
 
+// 256-wide tiles use eight epilogue warps (two per TMEM lane quadrant), so a
+// tile's epilogue takes half as long; 128-wide tiles keep four, which leaves
+// room for two resident blocks per SM at shallow rings.
 template <int BN, int STAGES>
-using Bf16Cfg = TcCfg<BN, STAGES, /*KC=*/0, /*BF16=*/1, /*INT_FOLD=*/false>;
+using Bf16Cfg = TcCfg<BN, STAGES, /*KC=*/0, /*BF16=*/1, /*INT_FOLD=*/false, BN == 256 ? 8 : 4>;
 
 template <int BN, int STAGES>
 static KernelInfo info_bf16() {

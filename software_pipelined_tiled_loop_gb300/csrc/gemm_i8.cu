@@ -21,19 +21,24 @@ namespace pg {
 
 constexpr int kI8ChunkTiles = 4;  // 4 K-tiles of 64 = 256 products per exact fp32 round
 
-template <int STAGES>
-using I8Cfg = TcCfg<128, STAGES, kI8ChunkTiles, /*BF16=*/0, /*INT_FOLD=*/true>;
+// Each epilogue thread keeps a 128-column row of int32 sums in registers:
+// 128-wide tiles use four epilogue warps, 256-wide tiles eight.
+template <int BN, int STAGES>
+using I8Cfg = TcCfg<BN, STAGES, kI8ChunkTiles, /*BF16=*/0, /*INT_FOLD=*/true, BN == 256 ? 8 : 4>;
 
-template <int STAGES>
+template <int BN, int STAGES>
 static KernelInfo info_i8() {
-    KernelInfo k = tc_info<I8Cfg<STAGES>>();
-    k.launch_i8 = launch_tc<I8Cfg<STAGES>, LaunchI8>;
+    KernelInfo k = tc_info<I8Cfg<BN, STAGES>>();
+    k.launch_i8 = launch_tc<I8Cfg<BN, STAGES>, LaunchI8>;
     return k;
 }
 
 const KernelInfo *i8_kernels(int *count) {
-    static const KernelInfo table[] = {info_i8<2>(), info_i8<3>(), info_i8<4>(), info_i8<5>(),
-                                       info_i8<6>()};
+    static const KernelInfo table[] = {
+        info_i8<256, 2>(), info_i8<256, 3>(), info_i8<256, 4>(),
+        info_i8<128, 2>(), info_i8<128, 3>(), info_i8<128, 4>(), info_i8<128, 5>(),
+        info_i8<128, 6>(),
+    };
     *count = static_cast<int>(sizeof(table) / sizeof(table[0]));
     return table;
 }

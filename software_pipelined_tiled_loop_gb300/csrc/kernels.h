@@ -29,6 +29,7 @@ struct LaunchCommon {
     int blocks_per_sm;  // resident blocks per SM for this kernel (occupancy query)
     const CUtensorMap *tmap_a;
     const CUtensorMap *tmap_b;
+    const CUtensorMap *tmap_c;  // C as a 32 x 32-box, 128-byte-swizzled map, or nullptr
     KernelCtx ctx;
 };
 
@@ -54,6 +55,7 @@ struct KernelInfo {
     // Operand boxes the tensor maps must be encoded with (elements, x = innermost).
     int a_box_x = 0, a_box_y = 0, b_box_x = 0, b_box_y = 0;
     bool a_swizzle128 = true, b_swizzle128 = true;
+    bool c_tma = false;  // the kernel can store C through a tensor map
     const void *func = nullptr;
     cudaError_t (*launch_bf16)(const LaunchBf16 &, cudaStream_t) = nullptr;
     cudaError_t (*launch_f32)(const LaunchF32 &, cudaStream_t) = nullptr;

@@ -55,20 +55,25 @@ namespace pg {
 
 // BN: tile width; STAGES: ring depth; KC: K-tiles per accumulation round (0 =
 // all of K); BF16: operand type (1 = bf16, 0 = fp16); INT_FOLD: exact-int8
-// epilogue (fold fp32 chunk sums into int32 registers).
-template <int BN_, int STAGES_, int KC_, int BF16_, bool INT_FOLD_>
+// epilogue (fold fp32 chunk sums into int32 registers); EPI: epilogue warps
+// (4: one per TMEM lane quadrant; 8: two per quadrant, each half the columns).
+template <int BN_, int STAGES_, int KC_, int BF16_, bool INT_FOLD_, int EPI_ = 4>
 struct TcCfg {
     static constexpr int BM = 128, BN = BN_, BK = 64, STAGES = STAGES_, KC = KC_;
     static constexpr int BF16 = BF16_;
     static constexpr bool INT_FOLD = INT_FOLD_;
+    static constexpr int EPI = EPI_;
+    static constexpr int EPI_COLS = BN * 4 / EPI;  // columns per epilogue warp
     using Scalar = typename std::conditional<INT_FOLD, int32_t, float>::type;
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGING_BYTES = EPI * 32 * 32 * 4;  // one 32x32 block per warp
     static constexpr int ACC_COLS = BN;        // fp32 accumulator: one TMEM column per n
     static constexpr int TMEM_COLS = 2 * BN;   // two accumulators
-    static constexpr int THREADS = 192;
-    static constexpr int BAR_OFFSET = STAGES * STAGE_BYTES;
+    static constexpr int THREADS = 64 + 32 * EPI;
+    static constexpr int STAGING_OFFSET = STAGES * STAGE_BYTES;
+    static constexpr int BAR_OFFSET = STAGING_OFFSET + STAGING_BYTES;
     static constexpr int NUM_BARS = 2 * STAGES + 5;
     static constexpr int USED = BAR_OFFSET + NUM_BARS * 8 + 16;
     // TMEM has 512 columns per SM: at most 512 / TMEM_COLS blocks may share an
@@ -77,21 +82,87 @@ struct TcCfg {
     static constexpr int MAX_BLOCKS = 512 / TMEM_COLS;
     static constexpr int SMEM_BYTES = smem_request(USED + 1024, MAX_BLOCKS);
     static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
-    static_assert(!INT_FOLD || BN == 128, "the int32 fold keeps one 128-column row per thread");
+    static_assert(EPI == 4 || EPI == 8, "EPI");
+    static_assert(EPI_COLS % 32 == 0, "epilogue column split");
+    static_assert(!INT_FOLD || EPI_COLS == 128, "the int32 fold keeps 128 columns per thread");
     static_assert(USED + 1024 <= 232448, "shared memory");
 };
 
+// One warp writes a 32 x 32 block of C: rows [m_base, m_base + 32), columns
+// [col, col + 32); lane t holds row m_base + t in vals[0..31] (raw
+// accumulator values as 32-bit patterns; have_acc = false means zeros).  The
+// block is staged in shared memory with the 128-byte swizzle (16-byte chunk
+// j of row t at chunk j ^ (t % 8): conflict-free), then either
+//   - written by one TMA bulk-tensor store (C describable by a tensor map and
+//     beta == 0; the store clips rows/columns outside C), or
+//   - written by 32 coalesced row stores (lane l writes column col + l),
+//     predicated at the edges, reading C first when beta != 0.
+template <typename Scalar>
+__device__ __forceinline__ void store_block32(const GemmArgs<Scalar, Scalar> &a,
+                                              const CUtensorMap *tmap_c, uint8_t *buf,
+                                              int m_base, int col, const uint32_t *vals,
+                                              bool have_acc, bool tma_path) {
+    const uint32_t lane = lane_id();
+    const uint32_t sbuf = smem_u32(buf);
+    if (tma_path) {
+        // the previous store of this warp must have finished reading the buffer
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const Scalar x = have_acc ? __builtin_bit_cast(Scalar, vals[4 * j + e]) : Scalar(0);
+                o[e] = __builtin_bit_cast(uint32_t, axpby(a.alpha, x, Scalar(0), Scalar(0)));
+            }
+            sts128(sbuf + lane * 128 + ((j ^ (lane & 7)) << 4), o[0], o[1], o[2], o[3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tmap_c, buf, col, m_base);
+            bulk_commit();
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t z = 0u;
+            sts128(sbuf + lane * 128 + ((j ^ (lane & 7)) << 4), have_acc ? vals[4 * j] : z,
+                   have_acc ? vals[4 * j + 1] : z, have_acc ? vals[4 * j + 2] : z,
+                   have_acc ? vals[4 * j + 3] : z);
+        }
+        __syncwarp();
+        const bool read_c = a.beta != Scalar(0);
+        const int c = col + static_cast<int>(lane);
+#pragma unroll 4
+        for (int r = 0; r < 32; ++r) {
+            const uint32_t w = lds32(sbuf + r * 128 + ((((lane >> 2) ^ (r & 7))) << 4) + (lane & 3) * 4);
+            const int row = m_base + r;
+            if (row < a.M && c < a.N) {
+                Scalar *cp = a.C + static_cast<long long>(row) * a.ldc + c;
+                const Scalar x = __builtin_bit_cast(Scalar, w);
+                *cp = read_c ? axpby(a.alpha, x, a.beta, *cp) : axpby(a.alpha, x, Scalar(0), Scalar(0));
+            }
+        }
+        __syncwarp();
+    }
+}
+
 template <class Cfg>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(Cfg::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b,
+                   const __grid_constant__ CUtensorMap tmap_c,
                    const GemmArgs<typename Cfg::Scalar, typename Cfg::Scalar> args,
                    const KernelCtx ctx) {
+    using Scalar = typename Cfg::Scalar;
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align_1024(smem_raw);
     uint8_t *sA = smem;
     uint8_t *sB = smem + STAGES * Cfg::A_BYTES;
+    uint8_t *sStage = smem + Cfg::STAGING_OFFSET;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Cfg::BAR_OFFSET);
     uint64_t *empty = full + STAGES;
     uint64_t *acc_full = empty + STAGES;  // [2]
@@ -105,13 +176,14 @@ __global__ void __launch_bounds__(192, 1)
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmap_a);
         prefetch_tmap(&tmap_b);
+        if (args.c_tma) prefetch_tmap(&tmap_c);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
-            mbar_init(&acc_empty[b], 4);
+            mbar_init(&acc_empty[b], Cfg::EPI);
         }
         mbar_init(mma_done, 1);
         fence_barrier_init();
@@ -196,19 +268,28 @@ __global__ void __launch_bounds__(192, 1)
             mbar_wait(mma_done, 0, ctx, kSiteMmaDone);
         }
     } else {
-        // ---------------- epilogue warps 2..5 ----------------
-        const uint32_t q = warp & 3u;  // the TMEM lane quadrant this warp may read
+        // ---------------- epilogue warps ----------------
+        const uint32_t e = warp - 2;            // epilogue warp index
+        const uint32_t q = warp & 3u;           // the TMEM lane quadrant this warp may read
+        const int col0 = static_cast<int>(e >> 2) * Cfg::EPI_COLS;  // its column range
+        uint8_t *buf = sStage + e * (32 * 32 * 4);
+        const bool tma_path = args.c_tma && args.beta == Scalar(0);
         uint32_t gr = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
             int m0, n0;
             tile_origin(tile, args.num_m_tiles, args.num_n_tiles, args.group_m, BM, BN, m0, n0);
-            const int row = m0 + static_cast<int>(q * 32 + lane);
+            const int m_base = m0 + static_cast<int>(q * 32);
             if constexpr (Cfg::INT_FOLD) {
-                // exact int8: sum the chunks' integer-valued fp32 partials in int32
-                uint32_t acc[BN];
+                // Exact int8: sum the chunks' integer-valued fp32 partials in
+                // int32.  For an integer-valued x with |x| <= 2^22, x + 1.5*2^23
+                // is exact and its bit pattern is 0x4B400000 + x, so each value
+                // costs one FADD and one IADD (no quarter-rate F2I); the
+                // 0x4B400000 of every round is subtracted once at the end.
+                constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+                uint32_t acc[Cfg::EPI_COLS];
 #pragma unroll
-                for (int j = 0; j < BN; ++j) acc[j] = 0u;
+                for (int j = 0; j < Cfg::EPI_COLS; ++j) acc[j] = 0u;
                 for (int r = 0; r < rounds; ++r, ++gr) {
                     const uint32_t ab = gr & 1u, aph = (gr >> 1) & 1u;
                     if (!mbar_wait(&acc_full[ab], aph, ctx, kSiteEpilogueFull)) {
@@ -216,50 +297,64 @@ __global__ void __launch_bounds__(192, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t t_row = tmem_base + ((q * 32u) << 16) + ab * Cfg::ACC_COLS;
+                    const uint32_t t_row =
+                        tmem_base + ((q * 32u) << 16) + ab * Cfg::ACC_COLS + col0;
 #pragma unroll
-                    for (int c = 0; c < BN; c += 32) {
-                        uint32_t v[32];
-                        tmem_ld_32x32b_x32(t_row + c, v);
+                    for (int c = 0; c < Cfg::EPI_COLS; c += 16) {
+                        uint32_t v[16];
+                        tmem_ld_32x32b_x16(t_row + c, v);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            acc[c + e] += static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[e])));
+                        for (int j = 0; j < 16; ++j)
+                            acc[c + j] += __float_as_uint(__uint_as_float(v[j]) + kMagic);
                     }
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&acc_empty[ab]);
                 }
                 if (!ok) break;
+                const uint32_t bias = static_cast<uint32_t>(rounds) * 0x4B400000u;  // mod 2^32
 #pragma unroll
-                for (int c = 0; c < BN; c += 32) store_row32(args, row, n0 + c, acc + c, true);
+                for (int j = 0; j < Cfg::EPI_COLS; ++j) acc[j] -= bias;
+#pragma unroll
+                for (int c = 0; c < Cfg::EPI_COLS; c += 32)
+                    store_block32(args, &tmap_c, buf, m_base, n0 + col0 + c, acc + c, rounds > 0,
+                                  tma_path);
             } else {
                 if (rounds > 0) {
                     const uint32_t ab = gr & 1u, aph = (gr >> 1) & 1u;
                     if (!mbar_wait(&acc_full[ab], aph, ctx, kSiteEpilogueFull)) break;
                     tc_fence_after();
-                    const uint32_t t_row = tmem_base + ((q * 32u) << 16) + ab * Cfg::ACC_COLS;
+                    const uint32_t t_row =
+                        tmem_base + ((q * 32u) << 16) + ab * Cfg::ACC_COLS + col0;
 #pragma unroll 1
-                    for (int c = 0; c < BN; c += 32) {
+                    for (int c = 0; c < Cfg::EPI_COLS; c += 32) {
                         uint32_t v[32];
                         tmem_ld_32x32b_x32(t_row + c, v);
                         tmem_ld_wait();
-                        store_row32(args, row, n0 + c, v, true);
+                        if (c + 32 >= Cfg::EPI_COLS) {
+                            // last TMEM read of this accumulator: hand it back
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&acc_empty[ab]);
+                        }
+                        store_block32(args, &tmap_c, buf, m_base, n0 + col0 + c, v, true, tma_path);
                     }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&acc_empty[ab]);
                     ++gr;
                 } else {
                     // K == 0: C = beta * C, tensor memory is never read
                     uint32_t zero[32];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) zero[e] = 0u;
+                    for (int j = 0; j < 32; ++j) zero[j] = 0u;
 #pragma unroll 1
-                    for (int c = 0; c < BN; c += 32) store_row32(args, row, n0 + c, zero, false);
+                    for (int c = 0; c < Cfg::EPI_COLS; c += 32)
+                        store_block32(args, &tmap_c, buf, m_base, n0 + col0 + c, zero, false,
+                                      tma_path);
                 }
             }
         }
+        if (lane == 0) bulk_wait_all();  // this warp's C stores have landed
+        __syncwarp();
     }
 
     // ---------------- teardown ----------------
@@ -287,13 +382,14 @@ static cudaError_t launch_tc(const P &p, cudaStream_t stream) {
     a.beta = p.beta;
     a.C = p.C;
     a.ldc = p.ldc;
+    a.c_tma = p.tmap_c != nullptr ? 1 : 0;
     const int tiles = a.num_m_tiles * a.num_n_tiles;
     const int per_sm = p.blocks_per_sm < Cfg::MAX_BLOCKS ? p.blocks_per_sm : Cfg::MAX_BLOCKS;
     int grid = p.sm_count * (per_sm > 0 ? per_sm : 1);
     if (grid > tiles) grid = tiles;
     if (grid < 1) return cudaSuccess;
-    tc_gemm_kernel<Cfg><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(*p.tmap_a, *p.tmap_b, a,
-                                                                         p.ctx);
+    tc_gemm_kernel<Cfg><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(
+        *p.tmap_a, *p.tmap_b, p.tmap_c != nullptr ? *p.tmap_c : *p.tmap_a, a, p.ctx);
     return cudaGetLastError();
 }
 
@@ -311,6 +407,7 @@ static KernelInfo tc_info() {
     k.b_box_x = 64;
     k.b_box_y = Cfg::BK;
     k.a_swizzle128 = k.b_swizzle128 = true;
+    k.c_tma = true;
     k.func = reinterpret_cast<const void *>(tc_gemm_kernel<Cfg>);
     return k;
 }
