@@ -64,7 +64,8 @@ typedef enum {
     PGEMM_ERR_UNSUPPORTED_DEVICE = 3,
     PGEMM_ERR_CUDA = 4,
     PGEMM_ERR_TIMEOUT = 5,
-    PGEMM_ERR_UNSUPPORTED_CONFIG = 6
+    PGEMM_ERR_UNSUPPORTED_CONFIG = 6,
+    PGEMM_ERR_TOO_LARGE = 7
 } pgemm_status;
 
 /* Data types, for the introspection calls. */
@@ -98,6 +99,37 @@ PGEMM_API pgemm_status gemm_bf16(int M, int N, int K, float alpha, const uint16_
  * at most 256, folded into int32. */
 PGEMM_API pgemm_status gemm_i8(int M, int N, int K, int32_t alpha, const int8_t *A, const int8_t *B,
                      int32_t beta, int32_t *C, pgemm_stream_t stream);
+
+/* Size of the fixed device scratch array that gemm_i8_noalloc uses. */
+#define PGEMM_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* gemm_i8 for callers that must not have the library allocate device memory.
+ * The pages have no counterpart: this is a deployment variant of gemm_i8.
+ *
+ * Some callers cannot allocate: a program that has handed all of the GPU's
+ * memory to its own allocator or runs under a fixed memory budget, or code on
+ * a path where an allocation call is not allowed or could block (cudaFree can
+ * synchronise the whole device).  gemm_i8 widens A and B to fp16 in
+ * stream-ordered scratch it allocates per call; this entry point instead
+ * widens them into one file-scope device array of PGEMM_NOALLOC_SCRATCH_BYTES
+ * (32 MiB), which every GPU that loads the library holds until the process
+ * exits.  It calls no cudaMalloc, cudaMallocAsync or cudaFree.
+ *
+ * Same arguments, semantics and results as gemm_i8 (bit-identical).  Limit:
+ * 2 * (M * round_up(K, 8) + K * round_up(N, 8)) bytes, each operand rounded
+ * up to 256 bytes, must fit in the array; larger problems return
+ * PGEMM_ERR_TOO_LARGE without doing anything.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls share the one array and it keeps the
+ * last call's contents (no byte of it needs to start at zero: every byte a
+ * call reads it has written first), so calls whose work overlaps on the GPU
+ * (different streams without ordering between them) race and give wrong
+ * results: order them on one stream, or with events. */
+PGEMM_API pgemm_status gemm_i8_noalloc(int M, int N, int K, int32_t alpha, const int8_t *A,
+                                       const int8_t *B, int32_t beta, int32_t *C,
+                                       pgemm_stream_t stream);
 
 /* The same three operations with an explicit configuration (cfg may be NULL
  * for the default).  Returns PGEMM_ERR_UNSUPPORTED_CONFIG for a configuration

@@ -19,7 +19,8 @@ __all__ = [
     "PgemmError", "lib", "library_path", "gemm_f32", "gemm_bf16", "gemm_i8", "gemm_f32_ex",
     "gemm_bf16_ex", "gemm_i8_ex", "pgemm_default_config", "pgemm_list_configs",
     "pgemm_kernel_attrs", "pgemm_get_device_status", "pgemm_selftest_wait_timeout",
-    "pgemm_status_string", "pgemm_version", "DTYPES", "STATUS", "EXPORTED",
+    "pgemm_status_string", "pgemm_version", "gemm_i8_noalloc", "NOALLOC_SCRATCH_BYTES",
+    "DTYPES", "STATUS", "EXPORTED",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -28,15 +29,17 @@ library_path = os.path.join(_HERE, "libpipegemm.so")
 STATUS = {
     0: "PGEMM_OK", 1: "PGEMM_ERR_INVALID_VALUE", 2: "PGEMM_ERR_MISALIGNED",
     3: "PGEMM_ERR_UNSUPPORTED_DEVICE", 4: "PGEMM_ERR_CUDA", 5: "PGEMM_ERR_TIMEOUT",
-    6: "PGEMM_ERR_UNSUPPORTED_CONFIG",
+    6: "PGEMM_ERR_UNSUPPORTED_CONFIG", 7: "PGEMM_ERR_TOO_LARGE",
 }
+# Size of the fixed device array gemm_i8_noalloc widens its operands into.
+NOALLOC_SCRATCH_BYTES = 32 << 20
 DTYPES = {"f32": 0, "bf16": 1, "i8": 2}
 # Every function include/pgemm.h declares.
 EXPORTED = [
     "gemm_f32", "gemm_bf16", "gemm_i8", "gemm_f32_ex", "gemm_bf16_ex", "gemm_i8_ex",
     "pgemm_default_config", "pgemm_list_configs", "pgemm_kernel_attrs",
     "pgemm_get_device_status", "pgemm_selftest_wait_timeout", "pgemm_status_string",
-    "pgemm_version",
+    "pgemm_version", "gemm_i8_noalloc",
 ]
 
 
@@ -68,6 +71,7 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
         "gemm_f32": [i, i, i, f, vp, vp, f, vp, vp],
         "gemm_bf16": [i, i, i, f, vp, vp, f, vp, vp],
         "gemm_i8": [i, i, i, i32, vp, vp, i32, vp, vp],
+        "gemm_i8_noalloc": [i, i, i, i32, vp, vp, i32, vp, vp],
         "gemm_f32_ex": [i, i, i, f, vp, vp, f, vp, cfgp, vp],
         "gemm_bf16_ex": [i, i, i, f, vp, vp, f, vp, cfgp, vp],
         "gemm_i8_ex": [i, i, i, i32, vp, vp, i32, vp, cfgp, vp],
@@ -158,6 +162,17 @@ def gemm_i8(M, N, K, alpha, A, B, beta, C, stream=None):
     """C (int32) <- alpha*A@B + beta*C with int8 A, B, exact modulo 2^32.  Asynchronous."""
     _check(lib().gemm_i8(M, N, K, int(alpha), _ptr(A), _ptr(B), int(beta), _ptr(C),
                          _stream(stream)), "gemm_i8")
+
+
+def gemm_i8_noalloc(M, N, K, alpha, A, B, beta, C, stream=None):
+    """gemm_i8 that allocates no device memory: for callers whose memory is
+    owned by their own allocator or budget, or who may not call an allocator
+    on this path.  Operands are widened into one fixed 32 MiB device array
+    shared by all calls (calls overlapping on the GPU race); larger problems
+    raise PgemmError(PGEMM_ERR_TOO_LARGE).  The first call on a device looks
+    up that array's address and should come before any stream capture."""
+    _check(lib().gemm_i8_noalloc(M, N, K, int(alpha), _ptr(A), _ptr(B), int(beta), _ptr(C),
+                                 _stream(stream)), "gemm_i8_noalloc")
 
 
 def gemm_f32_ex(M, N, K, alpha, A, B, beta, C, config=None, stream=None):

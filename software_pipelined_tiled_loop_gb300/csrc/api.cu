@@ -209,9 +209,13 @@ struct Scratch {
 
 enum class Kind { F32, BF16, I8 };
 
+// fixed_scratch: when given, operand repacking / widening uses this device
+// buffer of fixed_scratch_bytes instead of stream-ordered allocations, and a
+// problem that does not fit is rejected with PGEMM_ERR_TOO_LARGE.
 template <Kind KIND, typename In, typename Sc, typename Out>
 static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const In *B, Sc beta,
-                              Out *C, const pgemm_config *cfg_in, cudaStream_t stream) {
+                              Out *C, const pgemm_config *cfg_in, cudaStream_t stream,
+                              void *fixed_scratch = nullptr, long long fixed_scratch_bytes = 0) {
     if (M < 0 || N < 0 || K < 0) return PGEMM_ERR_INVALID_VALUE;
     if (M == 0 || N == 0) return PGEMM_OK;
     if (C == nullptr || (K > 0 && (A == nullptr || B == nullptr))) return PGEMM_ERR_INVALID_VALUE;
@@ -251,9 +255,15 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
             const long long b_ld2 = b_repack ? round_up(N, align_elems) : ldb;
             const long long a_bytes = a_repack ? round_up(a_ld2 * M * in_bytes, 256) : 0;
             const long long b_bytes = b_repack ? round_up(b_ld2 * K * in_bytes, 256) : 0;
-            if (cudaMallocAsync(&scratch.p, a_bytes + b_bytes, stream) != cudaSuccess)
-                return PGEMM_ERR_CUDA;
-            uint8_t *base = static_cast<uint8_t *>(scratch.p);
+            uint8_t *base = nullptr;
+            if (fixed_scratch != nullptr) {
+                if (a_bytes + b_bytes > fixed_scratch_bytes) return PGEMM_ERR_TOO_LARGE;
+                base = static_cast<uint8_t *>(fixed_scratch);
+            } else {
+                if (cudaMallocAsync(&scratch.p, a_bytes + b_bytes, stream) != cudaSuccess)
+                    return PGEMM_ERR_CUDA;
+                base = static_cast<uint8_t *>(scratch.p);
+            }
             cudaError_t e = cudaSuccess;
             if (a_repack) {
                 e = widen ? launch_widen_i8(reinterpret_cast<const int8_t *>(A), lda, base, a_ld2, M,
@@ -340,6 +350,15 @@ __global__ void selftest_wait_kernel(KernelCtx ctx) {
     }
     __syncthreads();
     if (threadIdx.x == 0) mbar_wait(&bar, 0, ctx, kSiteSelfTest);
+}
+
+// The int8 GEMM with its widened operands placed in a caller-supplied device
+// buffer (no allocation); used by the no-allocation entry point.
+pgemm_status gemm_i8_fixed_scratch(int M, int N, int K, int32_t alpha, const int8_t *A,
+                                   const int8_t *B, int32_t beta, int32_t *C, void *scratch,
+                                   long long scratch_bytes, cudaStream_t stream) {
+    return gemm_impl<Kind::I8>(M, N, K, alpha, A, B, beta, C, nullptr, stream, scratch,
+                               scratch_bytes);
 }
 
 }  // namespace pg
@@ -464,6 +483,7 @@ const char *pgemm_status_string(pgemm_status status) {
         case PGEMM_ERR_CUDA: return "CUDA error";
         case PGEMM_ERR_TIMEOUT: return "device wait timed out";
         case PGEMM_ERR_UNSUPPORTED_CONFIG: return "configuration not built";
+        case PGEMM_ERR_TOO_LARGE: return "problem exceeds the fixed scratch of gemm_i8_noalloc";
     }
     return "unknown status";
 }

@@ -1,0 +1,55 @@
+// gemm_i8_noalloc: the exact int8 GEMM without any device allocation.
+//
+// For callers that cannot let the library allocate device memory (their own
+// allocator owns the GPU's memory, a fixed memory budget, or a path where an
+// allocation call is not allowed or could block), the int8 operands are
+// widened to fp16 into one file-scope device array instead of stream-ordered
+// scratch.  The array is PGEMM_NOALLOC_SCRATCH_BYTES (32 MiB) and every GPU
+// that loads the library holds it until the process exits.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/pgemm.h"
+#include "kernels.h"
+
+namespace {
+
+// The widened A and B of the most recent call (shared by all calls).
+static __device__ __align__(256) unsigned char g_noalloc_scratch[PGEMM_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_setup_mu;
+void *g_scratch_addr[kMaxDevices] = {};
+
+// Device address of the array on the current device, looked up once per
+// device.  In host code the array's name stands for a host-side shadow, not
+// for device memory, so the kernels are given this address instead.
+pgemm_status scratch_address(void **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PGEMM_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return PGEMM_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    if (g_scratch_addr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+            return PGEMM_ERR_CUDA;
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return PGEMM_OK;
+}
+
+}  // namespace
+
+extern "C" pgemm_status gemm_i8_noalloc(int M, int N, int K, int32_t alpha, const int8_t *A,
+                                        const int8_t *B, int32_t beta, int32_t *C,
+                                        pgemm_stream_t stream) {
+    if (M < 0 || N < 0 || K < 0) return PGEMM_ERR_INVALID_VALUE;
+    if (M == 0 || N == 0) return PGEMM_OK;
+    void *scratch = nullptr;
+    const pgemm_status st = scratch_address(&scratch);
+    if (st != PGEMM_OK) return st;
+    return pg::gemm_i8_fixed_scratch(M, N, K, alpha, A, B, beta, C, scratch,
+                                     static_cast<long long>(PGEMM_NOALLOC_SCRATCH_BYTES), stream);
+}

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/pgemm.h"
 #include "ptx.cuh"
 
 namespace pg {
@@ -72,4 +73,12 @@ namespace pg {
 // int8 -> fp16 widening pass (gemm_i8.cu): dst rows of pitch dld elements.
 cudaError_t launch_widen_i8(const int8_t *src, long long sld, void *dst, long long dld, int rows,
                             int cols, int sm_count, cudaStream_t stream);
+}  // namespace pg
+
+namespace pg {
+// api.cu: the int8 GEMM using `scratch` (scratch_bytes long) for its widened
+// operands instead of allocating; PGEMM_ERR_TOO_LARGE if they do not fit.
+pgemm_status gemm_i8_fixed_scratch(int M, int N, int K, int32_t alpha, const int8_t *A,
+                                   const int8_t *B, int32_t beta, int32_t *C, void *scratch,
+                                   long long scratch_bytes, cudaStream_t stream);
 }  // namespace pg

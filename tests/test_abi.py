@@ -42,7 +42,7 @@ def test_no_stray_exports(L):
 
 
 def test_status_strings(L):
-    for code in range(7):
+    for code in range(8):
         assert pg.pgemm_status_string(code)
     assert pg.pgemm_version() >= 100
 
