@@ -23,6 +23,9 @@ const KernelInfo *bf16_kernels(int *count) {
         info_bf16<256, 2>(), info_bf16<256, 3>(), info_bf16<256, 4>(),
         info_bf16<128, 2>(), info_bf16<128, 3>(), info_bf16<128, 4>(),
         info_bf16<128, 5>(), info_bf16<128, 6>(),
+        // S = 1: one slot, load and compute strictly alternate (the unpipelined
+        // comparator: "kernel 10" of the SGEMM page)
+        info_bf16<256, 1>(), info_bf16<128, 1>(),
     };
     *count = static_cast<int>(sizeof(table) / sizeof(table[0]));
     return table;

@@ -267,8 +267,9 @@ static KernelInfo info_f32() {
 }
 
 const KernelInfo *f32_kernels(int *count) {
+    // S = 1 is the unpipelined comparator (load and compute strictly alternate)
     static const KernelInfo table[] = {info_f32<2>(), info_f32<3>(), info_f32<4>(), info_f32<5>(),
-                                       info_f32<6>()};
+                                       info_f32<6>(), info_f32<1>()};
     *count = static_cast<int>(sizeof(table) / sizeof(table[0]));
     return table;
 }

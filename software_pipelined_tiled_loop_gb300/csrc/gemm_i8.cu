@@ -35,9 +35,9 @@ static KernelInfo info_i8() {
 
 const KernelInfo *i8_kernels(int *count) {
     static const KernelInfo table[] = {
-        info_i8<256, 2>(), info_i8<256, 3>(), info_i8<256, 4>(),
+        info_i8<256, 1>(), info_i8<256, 2>(), info_i8<256, 3>(), info_i8<256, 4>(),
         info_i8<128, 2>(), info_i8<128, 3>(), info_i8<128, 4>(), info_i8<128, 5>(),
-        info_i8<128, 6>(),
+        info_i8<128, 6>(), info_i8<128, 1>(),
     };
     *count = static_cast<int>(sizeof(table) / sizeof(table[0]));
     return table;

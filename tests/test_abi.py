@@ -51,11 +51,12 @@ def test_list_configs(L):
     f32 = pg.pgemm_list_configs("f32")
     bf16 = pg.pgemm_list_configs("bf16")
     i8 = pg.pgemm_list_configs("i8")
-    # stage counts 2..6 are built for every dtype (the stage sweep)
+    # stage counts 2..6 are built for every dtype (the stage sweep), plus the
+    # S = 1 unpipelined comparator
     for cfgs in (f32, bf16, i8):
-        assert {c[3] for c in cfgs} == {2, 3, 4, 5, 6}
-    assert {c[3] for c in bf16 if c[1] == 128} == {2, 3, 4, 5, 6}
-    assert {c[3] for c in bf16 if c[1] == 256} == {2, 3, 4}
+        assert {c[3] for c in cfgs} == {1, 2, 3, 4, 5, 6}
+    assert {c[3] for c in bf16 if c[1] == 128} == {1, 2, 3, 4, 5, 6}
+    assert {c[3] for c in bf16 if c[1] == 256} == {1, 2, 3, 4}
 
 
 @pytest.mark.parametrize("fn", ["gemm_f32", "gemm_bf16", "gemm_i8"])
