@@ -235,7 +235,7 @@ def run_gpu_workload(name: str, steps: int, warmup: int, dist_ctx, with_e2e: boo
     res = {"dtype": dtype, "M": M, "N": N, "K": K, "alpha": alpha, "beta": beta,
            "ms_per_step": total_ms / steps, "ms_min": min(per_step_ms),
            "ms_median": statistics.median(per_step_ms),
-           "tflops": flops * steps * dist_ctx.world / (total_ms * 1e-3) / 1e12,
+           "tflops": aggregate_throughput(flops, steps, dist_ctx.world, total_ms),
            "per_gpu_tflops": flops * steps / (total_ms * 1e-3) / 1e12,
            "launches_per_step": 1 if dtype != "i8" else 3,
            "config": pg.pgemm_default_config(dtype, M, N, K), "clocks": clk}
@@ -367,16 +367,27 @@ def sweep(dtypes, steps, warmup, only_k=None):
 
 # ------------------------------------------------------------ distributed ---
 class DistCtx:
-    def __init__(self):
+    """One process per GPU (torchrun); replicas only: no data-path collective.
+
+    The process group serves the barrier around the timed region and the
+    max-over-ranks of the timing.  NCCL on GPUs, gloo where there is none
+    (the multi-rank logic is tested on CPU with gloo)."""
+
+    def __init__(self, backend: str | None = None):
         self.world = int(os.environ.get("WORLD_SIZE", "1"))
         self.rank = int(os.environ.get("RANK", "0"))
         self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
         self.pg = None
+        self.device = "cpu"
         if self.world > 1:
             import torch
             import torch.distributed as dist
-            torch.cuda.set_device(self.local_rank)
-            dist.init_process_group("nccl")
+            if backend is None:
+                backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if backend == "nccl":
+                torch.cuda.set_device(self.local_rank)
+                self.device = "cuda"
+            dist.init_process_group(backend)
             self.pg = dist
 
     def barrier(self):
@@ -387,13 +398,19 @@ class DistCtx:
         if not self.pg:
             return v
         import torch
-        t = torch.tensor([v], dtype=torch.float64, device="cuda")
+        t = torch.tensor([v], dtype=torch.float64, device=self.device)
         self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
         return float(t.item())
 
     def close(self):
         if self.pg:
             self.pg.destroy_process_group()
+
+
+def aggregate_throughput(flops_per_step: float, steps: int, world: int, max_total_ms: float) -> float:
+    """Whole-job throughput in TFLOP/s: the FLOPs every rank did, over the
+    slowest rank's time (each rank runs its own full replica)."""
+    return flops_per_step * steps * world / (max_total_ms * 1e-3) / 1e12
 
 
 # ------------------------------------------------------------------- main ---

@@ -12,6 +12,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <functional>
 #include <mutex>
 #include <unordered_map>
 
@@ -25,6 +26,7 @@ namespace pg {
 __device__ uint32_t g_status_word = 0;
 
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s per mbarrier wait
+
 constexpr int kMaxDevices = 64;
 
 struct KernelState {
@@ -245,6 +247,7 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
     long long a_ld = lda, b_ld = ldb;
     Scratch scratch;
     scratch.s = stream;
+    std::function<cudaError_t()> prepass;  // repack / widening launch, if any
     if (K > 0) {
         const long long align_elems = 16 / in_bytes;
         const bool widen = KIND == Kind::I8;
@@ -264,23 +267,30 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
                     return PGEMM_ERR_CUDA;
                 base = static_cast<uint8_t *>(scratch.p);
             }
-            cudaError_t e = cudaSuccess;
+            // The pre-pass is launched below, after every tensor map is encoded,
+            // so that the GEMM launch follows it with no host work in between.
+            prepass = [=, &d]() -> cudaError_t {
+                if (widen)  // int8 -> fp16 of both operands in one launch
+                    return launch_widen_i8_pair(reinterpret_cast<const int8_t *>(A), lda, base,
+                                                a_ld2, M, K, reinterpret_cast<const int8_t *>(B),
+                                                ldb, base + a_bytes, b_ld2, K, N, d->sm_count,
+                                                stream);
+                cudaError_t e = cudaSuccess;
+                if (a_repack)
+                    e = launch_repack(A, lda, base, a_ld2, M, K, in_bytes, d->sm_count, stream);
+                if (e == cudaSuccess && b_repack)
+                    e = launch_repack(B, ldb, base + a_bytes, b_ld2, K, N, in_bytes, d->sm_count,
+                                      stream);
+                return e;
+            };
             if (a_repack) {
-                e = widen ? launch_widen_i8(reinterpret_cast<const int8_t *>(A), lda, base, a_ld2, M,
-                                            K, d->sm_count, stream)
-                          : launch_repack(A, lda, base, a_ld2, M, K, in_bytes, d->sm_count, stream);
                 a_op = base;
                 a_ld = a_ld2;
             }
-            if (e == cudaSuccess && b_repack) {
-                e = widen ? launch_widen_i8(reinterpret_cast<const int8_t *>(B), ldb, base + a_bytes,
-                                            b_ld2, K, N, d->sm_count, stream)
-                          : launch_repack(B, ldb, base + a_bytes, b_ld2, K, N, in_bytes,
-                                          d->sm_count, stream);
+            if (b_repack) {
                 b_op = base + a_bytes;
                 b_ld = b_ld2;
             }
-            if (e != cudaSuccess) return PGEMM_ERR_CUDA;
         }
     }
 
@@ -314,7 +324,8 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
         if (encode_2d(&tc_map, ct, 4, C, N, M, N, 32, 32, true) == PGEMM_OK) tmap_c = &tc_map;
     }
 
-    cudaError_t e = cudaSuccess;
+    cudaError_t e = prepass ? prepass() : cudaSuccess;
+    if (e != cudaSuccess) return PGEMM_ERR_CUDA;
     KernelCtx ctx{d->status, kDefaultWaitLimitNs};
     if constexpr (KIND == Kind::F32) {
         LaunchF32 p{};

@@ -23,13 +23,13 @@ constexpr int kI8ChunkTiles = 4;  // 4 K-tiles of 64 = 256 products per exact fp
 
 // Each epilogue thread keeps a 128-column row of int32 sums in registers:
 // 128-wide tiles use four epilogue warps, 256-wide tiles eight.
-template <int BN, int STAGES>
-using I8Cfg = TcCfg<BN, STAGES, kI8ChunkTiles, /*BF16=*/0, /*INT_FOLD=*/true, BN == 256 ? 8 : 4>;
+template <int BN, int STAGES, int CM = 1>
+using I8Cfg = TcCfg<BN, STAGES, kI8ChunkTiles, /*BF16=*/0, /*INT_FOLD=*/true, BN == 256 ? 8 : 4, CM>;
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int CM = 1>
 static KernelInfo info_i8() {
-    KernelInfo k = tc_info<I8Cfg<BN, STAGES>>();
-    k.launch_i8 = launch_tc<I8Cfg<BN, STAGES>, LaunchI8>;
+    KernelInfo k = tc_info<I8Cfg<BN, STAGES, CM>>();
+    k.launch_i8 = launch_tc<I8Cfg<BN, STAGES, CM>, LaunchI8>;
     return k;
 }
 
@@ -38,58 +38,99 @@ const KernelInfo *i8_kernels(int *count) {
         info_i8<256, 1>(), info_i8<256, 2>(), info_i8<256, 3>(), info_i8<256, 4>(),
         info_i8<128, 2>(), info_i8<128, 3>(), info_i8<128, 4>(), info_i8<128, 5>(),
         info_i8<128, 6>(), info_i8<128, 1>(),
+        info_i8<256, 3, 2>(), info_i8<256, 4, 2>(),
     };
     *count = static_cast<int>(sizeof(table) / sizeof(table[0]));
     return table;
 }
 
-// dst[r][c] = (fp16) src[r][c] for r < rows, c < cols; src pitch `sld`
-// elements, dst pitch `dld` elements.  16 values per thread when both rows
-// are 16-byte aligned, else one value per thread.
-__global__ void widen_i8_to_f16_kernel(const int8_t *__restrict__ src, long long sld,
-                                       __half *__restrict__ dst, long long dld, int rows,
-                                       int cols, int vec) {
-    const long long per_row = vec ? (cols + 15) / 16 : cols;
-    const long long total = per_row * rows;
-    for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
-         idx < total; idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const long long r = idx / per_row;
-        const long long cc = idx - r * per_row;
-        if (vec) {
-            const int c0 = static_cast<int>(cc * 16);
-            const int8_t *s = src + r * sld + c0;
-            __half *d = dst + r * dld + c0;
-            if (c0 + 16 <= cols) {
-                const int4 v = *reinterpret_cast<const int4 *>(s);
-                const int8_t *b = reinterpret_cast<const int8_t *>(&v);
-                __align__(16) __half h[16];
+// Exact int8 -> fp16 for four packed bytes: bias each byte to b = x + 128,
+// place it under the fp16 exponent 0x64 (the fp16 value 1024 + b, exact), and
+// subtract 1152 with one half2 op: 1024 + x + 128 - 1152 = x, exact.
+__device__ __forceinline__ void widen4(uint32_t w, __half2 &lo, __half2 &hi) {
+    const uint32_t b = w ^ 0x80808080u;                    // x + 128 per byte
+    const uint32_t l = __byte_perm(b, 0x64646464u, 0x4140);  // [0x64 b1 | 0x64 b0]
+    const uint32_t h = __byte_perm(b, 0x64646464u, 0x4342);  // [0x64 b3 | 0x64 b2]
+    const __half2 bias = __half2half2(__ushort_as_half(0x6480));  // 1152.0
+    lo = __hsub2(*reinterpret_cast<const __half2 *>(&l), bias);
+    hi = __hsub2(*reinterpret_cast<const __half2 *>(&h), bias);
+}
+
+struct WidenJob {
+    const int8_t *src;
+    long long sld;   // source pitch (elements)
+    __half *dst;
+    long long dld;   // destination pitch (elements)
+    int rows, cols;
+    int vec;         // 1: 16-byte vectors (aligned rows, cols % 16 == 0)
+};
+
+// dst[r][c] = (fp16) src[r][c] for r < rows, c < cols, for the two operands
+// (blockIdx.y selects A or B).  32 values per thread per step on the vector
+// path, one value per thread otherwise.
+__global__ void __launch_bounds__(256) widen_i8_to_f16_kernel(WidenJob ja, WidenJob jb) {
+    const WidenJob &j = blockIdx.y == 0 ? ja : jb;
+    if (j.rows <= 0 || j.cols <= 0) return;
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    const long long t0 = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+    if (j.vec) {
+        const long long per_row = j.cols / 32 + ((j.cols % 32) ? 1 : 0);  // 32-wide pieces
+        const long long total = per_row * j.rows;
+        for (long long i = t0; i < total; i += stride) {
+            const long long r = i / per_row;
+            const int c0 = static_cast<int>(i - r * per_row) * 32;
+            const int8_t *s = j.src + r * j.sld + c0;
+            __half *d = j.dst + r * j.dld + c0;
+            const int nvec = min(2, (j.cols - c0) / 16);  // 16-value vectors in this piece
 #pragma unroll
-                for (int e = 0; e < 16; ++e) h[e] = __short2half_rn(static_cast<short>(b[e]));
-                reinterpret_cast<int4 *>(d)[0] = reinterpret_cast<const int4 *>(h)[0];
-                reinterpret_cast<int4 *>(d)[1] = reinterpret_cast<const int4 *>(h)[1];
-            } else {
-                for (int e = 0; c0 + e < cols; ++e) d[e] = __short2half_rn(static_cast<short>(s[e]));
+            for (int v = 0; v < 2; ++v) {
+                if (v < nvec) {
+                    const uint4 w = reinterpret_cast<const uint4 *>(s)[v];
+                    __half2 o[8];
+                    widen4(w.x, o[0], o[1]);
+                    widen4(w.y, o[2], o[3]);
+                    widen4(w.z, o[4], o[5]);
+                    widen4(w.w, o[6], o[7]);
+                    reinterpret_cast<uint4 *>(d)[2 * v] = *reinterpret_cast<const uint4 *>(&o[0]);
+                    reinterpret_cast<uint4 *>(d)[2 * v + 1] = *reinterpret_cast<const uint4 *>(&o[4]);
+                }
             }
-        } else {
-            dst[r * dld + cc] = __short2half_rn(static_cast<short>(src[r * sld + cc]));
+        }
+    } else {
+        const long long total = static_cast<long long>(j.rows) * j.cols;
+        for (long long i = t0; i < total; i += stride) {
+            const long long r = i / j.cols, c = i - r * j.cols;
+            j.dst[r * j.dld + c] = __short2half_rn(static_cast<short>(j.src[r * j.sld + c]));
         }
     }
 }
 
-cudaError_t launch_widen_i8(const int8_t *src, long long sld, void *dst, long long dld, int rows,
-                            int cols, int sm_count, cudaStream_t stream) {
-    if (rows <= 0 || cols <= 0) return cudaSuccess;
-    const int vec = ((reinterpret_cast<uintptr_t>(src) & 15u) == 0 && sld % 16 == 0 &&
-                     (reinterpret_cast<uintptr_t>(dst) & 15u) == 0 && dld % 8 == 0)
-                        ? 1
-                        : 0;
-    const long long per_row = vec ? (cols + 15) / 16 : cols;
-    const long long total = per_row * rows;
-    long long blocks = (total + 255) / 256;
-    const long long cap = static_cast<long long>(sm_count) * 8;
+static WidenJob make_job(const int8_t *src, long long sld, void *dst, long long dld, int rows,
+                         int cols) {
+    WidenJob j{src, sld, static_cast<__half *>(dst), dld, rows, cols, 0};
+    j.vec = ((reinterpret_cast<uintptr_t>(src) & 15u) == 0 && sld % 16 == 0 &&
+             (reinterpret_cast<uintptr_t>(dst) & 15u) == 0 && dld % 8 == 0 && cols % 16 == 0)
+                ? 1
+                : 0;
+    return j;
+}
+
+cudaError_t launch_widen_i8_pair(const int8_t *a, long long lda, void *a_dst, long long a_dld,
+                                 int a_rows, int a_cols, const int8_t *b, long long ldb,
+                                 void *b_dst, long long b_dld, int b_rows, int b_cols,
+                                 int sm_count, cudaStream_t stream) {
+    const WidenJob ja = make_job(a, lda, a_dst, a_dld, a_rows, a_cols);
+    const WidenJob jb = make_job(b, ldb, b_dst, b_dld, b_rows, b_cols);
+    auto work = [](const WidenJob &j) -> long long {
+        return j.vec ? (static_cast<long long>(j.cols) / 32 + 1) * j.rows
+                     : static_cast<long long>(j.rows) * j.cols;
+    };
+    long long items = work(ja) > work(jb) ? work(ja) : work(jb);
+    long long blocks = (items + 255) / 256;
+    const long long cap = static_cast<long long>(sm_count) * 16;
     if (blocks > cap) blocks = cap;
-    widen_i8_to_f16_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
-        src, sld, static_cast<__half *>(dst), dld, rows, cols, vec);
+    if (blocks < 1) blocks = 1;
+    widen_i8_to_f16_kernel<<<dim3(static_cast<unsigned>(blocks), 2), 256, 0, stream>>>(ja, jb);
     return cudaGetLastError();
 }
 

@@ -70,9 +70,12 @@ const KernelInfo *i8_kernels(int *count);
 }  // namespace pg
 
 namespace pg {
-// int8 -> fp16 widening pass (gemm_i8.cu): dst rows of pitch dld elements.
-cudaError_t launch_widen_i8(const int8_t *src, long long sld, void *dst, long long dld, int rows,
-                            int cols, int sm_count, cudaStream_t stream);
+// int8 -> fp16 widening of A and B in one launch (gemm_i8.cu); destination
+// rows have pitches a_dld / b_dld elements.
+cudaError_t launch_widen_i8_pair(const int8_t *a, long long lda, void *a_dst, long long a_dld,
+                                 int a_rows, int a_cols, const int8_t *b, long long ldb,
+                                 void *b_dst, long long b_dld, int b_rows, int b_cols,
+                                 int sm_count, cudaStream_t stream);
 }  // namespace pg
 
 namespace pg {

@@ -169,6 +169,31 @@ __device__ __forceinline__ uint32_t lds32(uint32_t saddr) {
     return v;
 }
 
+// As tma_load_2d, but the box is written to the same shared-memory offset in
+// every CTA of the cluster named in `cta_mask`, and each of them gets the
+// transaction bytes on its own barrier at `bar`'s offset.
+__device__ __forceinline__ void tma_load_2d_multicast(void *smem_dst, const CUtensorMap *map,
+                                                      uint64_t *bar, int32_t x, int32_t y,
+                                                      uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(cta_mask)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Barrier over every thread of every CTA in the cluster (release / acquire).
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                     "memory");
+}
+
 // Order this thread's generic-proxy shared-memory accesses before later
 // async-proxy (TMA / tcgen05) accesses of the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -220,6 +245,16 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
             smem_u32(bar))
+        : "memory");
+}
+
+// As umma_commit, arriving on the barrier at `bar`'s offset in every CTA of
+// the cluster named in `cta_mask`.
+__device__ __forceinline__ void umma_commit_multicast(uint64_t *bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_u32(bar)),
+        "h"(cta_mask)
         : "memory");
 }
 

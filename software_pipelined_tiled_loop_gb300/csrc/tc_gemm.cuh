@@ -57,9 +57,12 @@ namespace pg {
 // all of K); BF16: operand type (1 = bf16, 0 = fp16); INT_FOLD: exact-int8
 // epilogue (fold fp32 chunk sums into int32 registers); EPI: epilogue warps
 // (4: one per TMEM lane quadrant; 8: two per quadrant, each half the columns).
-template <int BN_, int STAGES_, int KC_, int BF16_, bool INT_FOLD_, int EPI_ = 4>
+// CM: CTAs per cluster along M (1, or 2: the pair computes two vertically
+// adjacent tiles and shares one B panel, each CTA loading half of it by TMA
+// multicast into both CTAs' shared memory).
+template <int BN_, int STAGES_, int KC_, int BF16_, bool INT_FOLD_, int EPI_ = 4, int CM_ = 1>
 struct TcCfg {
-    static constexpr int BM = 128, BN = BN_, BK = 64, STAGES = STAGES_, KC = KC_;
+    static constexpr int BM = 128, BN = BN_, BK = 64, STAGES = STAGES_, KC = KC_, CM = CM_;
     static constexpr int BF16 = BF16_;
     static constexpr bool INT_FOLD = INT_FOLD_;
     static constexpr int EPI = EPI_;
@@ -86,6 +89,7 @@ struct TcCfg {
     static_assert(EPI_COLS % 32 == 0, "epilogue column split");
     static_assert(!INT_FOLD || EPI_COLS == 128, "the int32 fold keeps 128 columns per thread");
     static_assert(USED + 1024 <= 232448, "shared memory");
+    static_assert(CM == 1 || (CM == 2 && (BN / 64) % 2 == 0), "cluster split of B");
 };
 
 // One warp writes a 32 x 32 block of C: rows [m_base, m_base + 32), columns
@@ -179,7 +183,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         if (args.c_tma) prefetch_tmap(&tmap_c);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            // released by the MMA issuer of every CTA whose B half lands here
+            mbar_init(&empty[s], Cfg::CM);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
@@ -193,11 +198,21 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         tmem_relinquish();
     }
     tc_fence_before();
-    __syncthreads();
+    __syncwarp();
+    if constexpr (Cfg::CM > 1)
+        cluster_sync();  // the peer's barriers exist before any multicast reaches them
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int num_tiles = args.num_m_tiles * args.num_n_tiles;
+    // Cluster geometry: with CM > 1 a "tile" of the schedule is a CM x 1 stack
+    // of output tiles; this CTA computes the one at its cluster rank.
+    const uint32_t crank = Cfg::CM > 1 ? cluster_ctarank() : 0u;
+    const int sched_id = static_cast<int>(blockIdx.x) / Cfg::CM;
+    const int sched_stride = static_cast<int>(gridDim.x) / Cfg::CM;
+    const int num_m_sched = (args.num_m_tiles + Cfg::CM - 1) / Cfg::CM;
+    const int num_tiles = num_m_sched * args.num_n_tiles;
     const int T = args.num_k_tiles;
     // accumulation rounds per output tile
     const int KCt = Cfg::KC > 0 ? Cfg::KC : (T > 0 ? T : 1);
@@ -208,9 +223,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             // ---------------- producer: TMA into the stage ring ----------------
             uint32_t it = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            for (int tile = sched_id; ok && tile < num_tiles; tile += sched_stride) {
                 int m0, n0;
-                tile_origin(tile, args.num_m_tiles, args.num_n_tiles, args.group_m, BM, BN, m0, n0);
+                tile_origin(tile, num_m_sched, args.num_n_tiles, args.group_m, BM * Cfg::CM, BN, m0,
+                            n0);
+                m0 += static_cast<int>(crank) * BM;
                 for (int kt = 0; kt < T; ++kt, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
                     if (!mbar_wait(&empty[s], ph ^ 1u, ctx, kSiteProducerEmpty)) {
@@ -219,10 +236,31 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     }
                     mbar_arrive_expect_tx(&full[s], Cfg::STAGE_BYTES);
                     tma_load_2d(sA + s * Cfg::A_BYTES, &tmap_a, &full[s], kt * BK, m0);
+                    if constexpr (Cfg::CM == 1) {
 #pragma unroll
-                    for (int j = 0; j < BN / 64; ++j)
-                        tma_load_2d(sB + s * Cfg::B_BYTES + j * (BK * 128), &tmap_b, &full[s],
-                                    n0 + j * 64, kt * BK);
+                        for (int j = 0; j < BN / 64; ++j)
+                            tma_load_2d(sB + s * Cfg::B_BYTES + j * (BK * 128), &tmap_b, &full[s],
+                                        n0 + j * 64, kt * BK);
+                    } else {
+                        // this CTA's share of the B boxes, written into every CTA of the pair
+                        constexpr int JB = BN / 64 / Cfg::CM;
+#pragma unroll
+                        for (int jj = 0; jj < JB; ++jj) {
+                            const int j = static_cast<int>(crank) * JB + jj;
+                            tma_load_2d_multicast(sB + s * Cfg::B_BYTES + j * (BK * 128), &tmap_b,
+                                                  &full[s], n0 + j * 64, kt * BK,
+                                                  static_cast<uint16_t>((1u << Cfg::CM) - 1u));
+                        }
+                    }
+                }
+            }
+            if constexpr (Cfg::CM > 1) {
+                // Producer tail: wait for the last release of every stage.  That
+                // includes the peer MMA issuer's multicast arrivals on this CTA's
+                // barriers, so none can land after the cluster has been left.
+                for (int i = 0; ok && i < STAGES; ++i, ++it) {
+                    const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+                    ok = mbar_wait(&empty[s], ph ^ 1u, ctx, kSiteProducerEmpty);
                 }
             }
         }
@@ -233,7 +271,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                                                  /*B N-major*/ 1);
             uint32_t it = 0, gr = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            for (int tile = sched_id; ok && tile < num_tiles; tile += sched_stride) {
                 for (int r = 0; ok && r < rounds; ++r, ++gr) {
                     const uint32_t ab = gr & 1u, aph = (gr >> 1) & 1u;
                     if (!mbar_wait(&acc_empty[ab], aph ^ 1u, ctx, kSiteMmaAccEmpty)) {
@@ -259,7 +297,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                             const uint64_t bd = smem_desc_sw128(b_addr + k * 2048, BK * 128, 1024);
                             umma_f16_ss(d_tmem, ad, bd, idesc, (first && k == 0) ? 0u : 1u);
                         }
-                        umma_commit(&empty[s]);  // stage s is free once these MMAs read it
+                        // stage s is free once these MMAs have read it (in every CTA whose
+                        // producer wrote into it)
+                        if constexpr (Cfg::CM == 1)
+                            umma_commit(&empty[s]);
+                        else
+                            umma_commit_multicast(&empty[s], static_cast<uint16_t>((1u << Cfg::CM) - 1u));
                     }
                     if (ok) umma_commit(&acc_full[ab]);  // round complete -> epilogue
                 }
@@ -276,9 +319,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         const bool tma_path = args.c_tma && args.beta == Scalar(0);
         uint32_t gr = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        for (int tile = sched_id; ok && tile < num_tiles; tile += sched_stride) {
             int m0, n0;
-            tile_origin(tile, args.num_m_tiles, args.num_n_tiles, args.group_m, BM, BN, m0, n0);
+            tile_origin(tile, num_m_sched, args.num_n_tiles, args.group_m, BM * Cfg::CM, BN, m0, n0);
+            m0 += static_cast<int>(crank) * BM;
+            const bool in_range = m0 < args.M;  // the second tile of a pair may lie below C
             const int m_base = m0 + static_cast<int>(q * 32);
             if constexpr (Cfg::INT_FOLD) {
                 // Exact int8: sum the chunks' integer-valued fp32 partials in
@@ -316,10 +361,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 const uint32_t bias = static_cast<uint32_t>(rounds) * 0x4B400000u;  // mod 2^32
 #pragma unroll
                 for (int j = 0; j < Cfg::EPI_COLS; ++j) acc[j] -= bias;
+                if (in_range) {
 #pragma unroll
-                for (int c = 0; c < Cfg::EPI_COLS; c += 32)
-                    store_block32(args, &tmap_c, buf, m_base, n0 + col0 + c, acc + c, rounds > 0,
-                                  tma_path);
+                    for (int c = 0; c < Cfg::EPI_COLS; c += 32)
+                        store_block32(args, &tmap_c, buf, m_base, n0 + col0 + c, acc + c,
+                                      rounds > 0, tma_path);
+                }
             } else {
                 if (rounds > 0) {
                     const uint32_t ab = gr & 1u, aph = (gr >> 1) & 1u;
@@ -338,7 +385,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                             __syncwarp();
                             if (lane == 0) mbar_arrive(&acc_empty[ab]);
                         }
-                        store_block32(args, &tmap_c, buf, m_base, n0 + col0 + c, v, true, tma_path);
+                        if (in_range)
+                            store_block32(args, &tmap_c, buf, m_base, n0 + col0 + c, v, true,
+                                          tma_path);
                     }
                     ++gr;
                 } else {
@@ -347,7 +396,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 #pragma unroll
                     for (int j = 0; j < 32; ++j) zero[j] = 0u;
 #pragma unroll 1
-                    for (int c = 0; c < Cfg::EPI_COLS; c += 32)
+                    for (int c = 0; in_range && c < Cfg::EPI_COLS; c += 32)
                         store_block32(args, &tmap_c, buf, m_base, n0 + col0 + c, zero, false,
                                       tma_path);
                 }
@@ -359,7 +408,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 
     // ---------------- teardown ----------------
     tc_fence_before();
-    __syncthreads();
+    __syncwarp();
+    if constexpr (Cfg::CM > 1)
+        cluster_sync();  // no CTA leaves while its peer may still write into it
+    else
+        __syncthreads();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
@@ -383,20 +436,46 @@ static cudaError_t launch_tc(const P &p, cudaStream_t stream) {
     a.C = p.C;
     a.ldc = p.ldc;
     a.c_tma = p.tmap_c != nullptr ? 1 : 0;
-    const int tiles = a.num_m_tiles * a.num_n_tiles;
-    const int per_sm = p.blocks_per_sm < Cfg::MAX_BLOCKS ? p.blocks_per_sm : Cfg::MAX_BLOCKS;
-    int grid = p.sm_count * (per_sm > 0 ? per_sm : 1);
-    if (grid > tiles) grid = tiles;
-    if (grid < 1) return cudaSuccess;
-    tc_gemm_kernel<Cfg><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(
-        *p.tmap_a, *p.tmap_b, p.tmap_c != nullptr ? *p.tmap_c : *p.tmap_a, a, p.ctx);
-    return cudaGetLastError();
+    const CUtensorMap &tc = p.tmap_c != nullptr ? *p.tmap_c : *p.tmap_a;
+    if constexpr (Cfg::CM == 1) {
+        const int tiles = a.num_m_tiles * a.num_n_tiles;
+        const int per_sm = p.blocks_per_sm < Cfg::MAX_BLOCKS ? p.blocks_per_sm : Cfg::MAX_BLOCKS;
+        int grid = p.sm_count * (per_sm > 0 ? per_sm : 1);
+        if (grid > tiles) grid = tiles;
+        if (grid < 1) return cudaSuccess;
+        tc_gemm_kernel<Cfg><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(*p.tmap_a, *p.tmap_b,
+                                                                             tc, a, p.ctx);
+        return cudaGetLastError();
+    } else {
+        // clusters of CM CTAs; as many as can be resident at once (persistent)
+        const int sched_tiles = ((a.num_m_tiles + Cfg::CM - 1) / Cfg::CM) * a.num_n_tiles;
+        cudaLaunchConfig_t lc{};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = Cfg::CM;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        lc.blockDim = dim3(Cfg::THREADS);
+        lc.dynamicSmemBytes = Cfg::SMEM_BYTES;
+        lc.stream = stream;
+        lc.attrs = attr;
+        lc.numAttrs = 1;
+        int clusters = 0;
+        lc.gridDim = dim3(Cfg::CM * p.sm_count);
+        cudaError_t e = cudaOccupancyMaxActiveClusters(&clusters, tc_gemm_kernel<Cfg>, &lc);
+        if (e != cudaSuccess) return e;
+        if (clusters < 1) return cudaErrorInvalidConfiguration;
+        if (clusters > sched_tiles) clusters = sched_tiles;
+        if (clusters < 1) return cudaSuccess;
+        lc.gridDim = dim3(Cfg::CM * clusters);
+        return cudaLaunchKernelEx(&lc, tc_gemm_kernel<Cfg>, *p.tmap_a, *p.tmap_b, tc, a, p.ctx);
+    }
 }
 
 template <class Cfg>
 static KernelInfo tc_info() {
     KernelInfo k;
-    k.bm = Cfg::BM;
+    k.bm = Cfg::BM * Cfg::CM;  // the tile a cluster computes
     k.bn = Cfg::BN;
     k.bk = Cfg::BK;
     k.stages = Cfg::STAGES;
