@@ -46,9 +46,11 @@
 
 namespace pg {
 
-template <int STAGES>
+template <int BN_, int STAGES>
 struct F32Cfg {
-    static constexpr int BM = 128, BN = 128, BK = 32;
+    static constexpr int BM = 128, BN = BN_, BK = 32;
+    static constexpr int G = BN / 32;             // float4 column groups per thread
+    static constexpr int MIN_BLOCKS = BN == 64 ? 3 : 2;  // register budget per thread
     static constexpr int A_BYTES = BM * BK * 4;  // 16 KB
     static constexpr int B_BYTES = BK * BN * 4;  // 16 KB
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -58,6 +60,7 @@ struct F32Cfg {
     static constexpr int USED = BAR_OFFSET + 2 * STAGES * 8;
     static constexpr int SMEM_BYTES = USED + 1024;
     static_assert(SMEM_BYTES <= 232448, "shared memory");
+    static_assert(BN == 64 || BN == 128, "BN");
 };
 
 __device__ __forceinline__ float4 lds128(uint32_t saddr) {
@@ -68,12 +71,13 @@ __device__ __forceinline__ float4 lds128(uint32_t saddr) {
     return v;
 }
 
-template <int STAGES>
-__global__ void __launch_bounds__(128, 2)
+template <int BN_, int STAGES>
+__global__ void __launch_bounds__(128, F32Cfg<BN_, STAGES>::MIN_BLOCKS)
     gemm_f32_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_b,
                     const GemmArgs<float, float> args, const KernelCtx ctx) {
-    using Cfg = F32Cfg<STAGES>;
+    using Cfg = F32Cfg<BN_, STAGES>;
+    constexpr int G = Cfg::G;
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align_1024(smem_raw);
@@ -121,15 +125,17 @@ __global__ void __launch_bounds__(128, 2)
     const int tc = static_cast<int>(lane) & 3;   // 0..3
 
     // acc[i][2*g + h] holds columns 16*g + 4*tc + 2*h + {0,1} of row 8*i + tr
-    float2 acc[8][8];
+    // (within this warp's WN = BN/2 columns)
+    constexpr int WN = BN / 2;
+    float2 acc[8][2 * G];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = make_float2(0.f, 0.f);
+        for (int j = 0; j < 2 * G; ++j) acc[i][j] = make_float2(0.f, 0.f);
 
     // byte offsets inside a slot
     const uint32_t a_row0 = static_cast<uint32_t>((wm * 64 + tr) * 128);  // row 8*i+tr: + i*1024
-    const uint32_t b_col0 = static_cast<uint32_t>((wn * 64 + tc * 4) * 4);
+    const uint32_t b_col0 = static_cast<uint32_t>((wn * WN + tc * 4) * 4);
 
     bool ok = true;
     for (int kt = 0; kt < T; ++kt) {
@@ -161,16 +167,16 @@ __global__ void __launch_bounds__(128, 2)
                 a[i] = lds128(a_base + i * 1024 + ((k4 ^ tr) << 4));
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-                float4 b[4];
+                float4 b[G];
                 const uint32_t brow = b_base + (k4 * 4 + kk) * (BN * 4);
 #pragma unroll
-                for (int g = 0; g < 4; ++g) b[g] = lds128(brow + g * 64);
+                for (int g = 0; g < G; ++g) b[g] = lds128(brow + g * 64);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
                     const float2 a2 = make_float2(av, av);
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) {
+                    for (int g = 0; g < G; ++g) {
                         acc[i][2 * g] = __ffma2_rn(a2, make_float2(b[g].x, b[g].y), acc[i][2 * g]);
                         acc[i][2 * g + 1] =
                             __ffma2_rn(a2, make_float2(b[g].z, b[g].w), acc[i][2 * g + 1]);
@@ -193,8 +199,8 @@ __global__ void __launch_bounds__(128, 2)
         if (row >= args.M) continue;
         float *crow = args.C + static_cast<long long>(row) * args.ldc;
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-            const int col = n0 + wn * 64 + 16 * g + 4 * tc;
+        for (int g = 0; g < G; ++g) {
+            const int col = n0 + wn * WN + 16 * g + 4 * tc;
             float *cp = crow + col;
             const float v[4] = {acc[i][2 * g].x, acc[i][2 * g].y, acc[i][2 * g + 1].x,
                                 acc[i][2 * g + 1].y};
@@ -223,9 +229,9 @@ __global__ void __launch_bounds__(128, 2)
 }
 
 // ----------------------------------------------------------------- host ---
-template <int STAGES>
+template <int BN, int STAGES>
 static cudaError_t launch_f32_impl(const LaunchF32 &p, cudaStream_t stream) {
-    using Cfg = F32Cfg<STAGES>;
+    using Cfg = F32Cfg<BN, STAGES>;
     GemmArgs<float, float> a{};
     a.M = p.M;
     a.N = p.N;
@@ -240,14 +246,14 @@ static cudaError_t launch_f32_impl(const LaunchF32 &p, cudaStream_t stream) {
     a.ldc = p.ldc;
     const int tiles = a.num_m_tiles * a.num_n_tiles;
     if (tiles < 1) return cudaSuccess;
-    gemm_f32_kernel<STAGES><<<tiles, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(*p.tmap_a, *p.tmap_b,
-                                                                             a, p.ctx);
+    gemm_f32_kernel<BN, STAGES><<<tiles, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(
+        *p.tmap_a, *p.tmap_b, a, p.ctx);
     return cudaGetLastError();
 }
 
-template <int STAGES>
+template <int BN, int STAGES>
 static KernelInfo info_f32() {
-    using Cfg = F32Cfg<STAGES>;
+    using Cfg = F32Cfg<BN, STAGES>;
     KernelInfo k;
     k.bm = Cfg::BM;
     k.bn = Cfg::BN;
@@ -257,19 +263,22 @@ static KernelInfo info_f32() {
     k.smem_bytes = Cfg::SMEM_BYTES;
     k.a_box_x = Cfg::BK;   // 32 floats = 128 bytes, swizzled
     k.a_box_y = Cfg::BM;
-    k.b_box_x = Cfg::BN;   // 128 floats = 512 bytes, unswizzled
+    k.b_box_x = Cfg::BN;   // BN floats (256 or 512 bytes), unswizzled
     k.b_box_y = Cfg::BK;
     k.a_swizzle128 = true;
     k.b_swizzle128 = false;
-    k.func = reinterpret_cast<const void *>(gemm_f32_kernel<STAGES>);
-    k.launch_f32 = launch_f32_impl<STAGES>;
+    k.func = reinterpret_cast<const void *>(gemm_f32_kernel<BN, STAGES>);
+    k.launch_f32 = launch_f32_impl<BN, STAGES>;
     return k;
 }
 
 const KernelInfo *f32_kernels(int *count) {
     // S = 1 is the unpipelined comparator (load and compute strictly alternate)
-    static const KernelInfo table[] = {info_f32<2>(), info_f32<3>(), info_f32<4>(), info_f32<5>(),
-                                       info_f32<6>(), info_f32<1>()};
+    static const KernelInfo table[] = {
+        info_f32<128, 2>(), info_f32<128, 3>(), info_f32<128, 4>(), info_f32<128, 5>(),
+        info_f32<128, 6>(), info_f32<128, 1>(),
+        // 128 x 64 tiles: 8 x 8 per thread, few enough registers for three blocks per SM
+        info_f32<64, 2>(), info_f32<64, 3>(), info_f32<64, 4>()};
     *count = static_cast<int>(sizeof(table) / sizeof(table[0]));
     return table;
 }

@@ -10,7 +10,7 @@
 
 #include <mutex>
 
-#include "../../include/pgemm.h"
+#include "pgemm.h"
 #include "kernels.h"
 
 namespace {

@@ -6,7 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/pgemm.h"
+#include "pgemm.h"
 #include "ptx.cuh"
 
 namespace pg {
