@@ -365,6 +365,75 @@ def sweep(dtypes, steps, warmup, only_k=None):
                 print(json.dumps(run_point(dtype, M, N, K, recipe, cfg, steps, warmup)), flush=True)
 
 
+# ----------------------------------------------------- stage-reuse hazard ---
+def hazard_stress(iters: int, delay_ns: int = 2000) -> dict:
+    """Run the two-stage copy-and-reduce with and without the
+    consume-before-reuse wait `iters` times each on a 4096 x 4096 integer
+    array with a fresh random row order every iteration and consumer warp 0
+    slowed by delay_ns per tile; count wrong row sums against the exact host
+    sums, and pull one annotated overwrite out of the hazard run's trace."""
+    import torch
+
+    import software_pipelined_tiled_loop_gb300 as pg
+    rows = cols = 4096
+    X = si.small_int_f32((rows, cols), 77, -8, 7)
+    rowsum = X.astype(np.int64).sum(axis=1)
+    dX = torch.from_numpy(X).cuda()
+    out = torch.zeros(rows, dtype=torch.float32, device="cuda")
+    cap = 8192
+    tr = torch.zeros(1 + 2 * cap, dtype=torch.int64, device="cuda")
+    rng = np.random.default_rng(0x5EED)
+    res = {}
+    for check in (1, 0):
+        fails, bad_rows, ms = 0, [], []
+        for it in range(iters):
+            perm = rng.permutation(rows).astype(np.int32)
+            dperm = torch.from_numpy(perm).cuda()
+            out.zero_()
+            tr.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            pg.pgemm_stage_reuse_demo(dX, rows, cols, dperm, out, check, 0, delay_ns,
+                                      tr if it == 0 else None, cap if it == 0 else 0)
+            e1.record()
+            torch.cuda.synchronize()
+            ms.append(e0.elapsed_time(e1))
+            bad = int(np.count_nonzero(out.cpu().numpy().astype(np.int64) != rowsum[perm]))
+            bad_rows.append(bad)
+            fails += bad > 0
+            if it == 0:
+                trace = tr.cpu().numpy().view(np.uint64).copy()
+        status = pg.pgemm_get_device_status()
+        name = "with_reuse_wait" if check else "without_reuse_wait"
+        res[name] = {"iterations": iters, "iterations_with_wrong_rows": fails,
+                     "wrong_rows_total": int(sum(bad_rows)), "wrong_rows_max": int(max(bad_rows)),
+                     "ms_median": round(statistics.median(ms), 4),
+                     "GB_per_s": round(rows * cols * 4 / (statistics.median(ms) * 1e-3) / 1e9, 1),
+                     "device_status": status, "timeline": _timeline_excerpt(trace, check)}
+    res["delay_ns_warp0"] = delay_ns
+    return res
+
+
+def _timeline_excerpt(tr, check):
+    """A few events around one stage reuse of block 0, times in ns from the first event."""
+    names = {1: "load issued", 2: "load landed", 3: "reuse wait begins", 4: "reuse allowed",
+             5: "read begins", 6: "read ends"}
+    n = int(tr[0])
+    ev = sorted((int(tr[1 + 2 * i]), int(tr[2 + 2 * i]) >> 56, (int(tr[2 + 2 * i]) >> 48) & 0xFF,
+                 (int(tr[2 + 2 * i]) >> 40) & 0xFF, int(tr[2 + 2 * i]) & 0xFFFFFFFF)
+                for i in range(min(n, (len(tr) - 1) // 2)))
+    if not ev:
+        return []
+    t0 = ev[0][0]
+    # around tile 4 of stage 0: its load, the reads of tile 2 (same stage) by every warp
+    keep = [e for e in ev if e[4] in (2, 4) and e[2] == 0]
+    if not check:
+        # the overwrite: tile 4's load landing before warp 0 has begun reading tile 2
+        keep = [e for e in ev if (e[4] == 4 and e[1] in (1, 2)) or (e[4] == 2 and e[1] in (5, 6))]
+    return [f"{e[0] - t0:>8d} ns  tile {e[4]} stage {e[2]} warp {e[3]}: {names.get(e[1], e[1])}"
+            for e in keep[:24]]
+
+
 # ------------------------------------------------------------ distributed ---
 class DistCtx:
     """One process per GPU (torchrun); replicas only: no data-path collective.
@@ -430,11 +499,18 @@ def main():
                     help="comma list of dtypes: time every built (tile, stages) config on the "
                          "sweep shapes, one JSON line per point")
     ap.add_argument("--sweep-k", default=None, help="comma list of K values to restrict the sweep")
+    ap.add_argument("--hazard", type=int, default=0,
+                    help="run the stage-reuse hazard experiment this many iterations per variant")
     ap.add_argument("--point", default=None,
                     help="dtype,M,N,K,bm,bn,bk,stages: time one point (for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
+    if args.hazard:
+        from software_pipelined_tiled_loop_gb300 import build as pgbuild
+        pgbuild.build()
+        print(json.dumps(hazard_stress(args.hazard)))
+        return
     if args.sweep or args.point:
         from software_pipelined_tiled_loop_gb300 import build as pgbuild
         pgbuild.build()

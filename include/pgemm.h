@@ -156,6 +156,26 @@ PGEMM_API pgemm_status pgemm_kernel_attrs(pgemm_dtype dtype, const pgemm_config 
                                 int *regs_per_thread, int *threads_per_block,
                                 int *blocks_per_sm);
 
+/* The stage-reuse hazard experiment of "Software pipelines and asynchronous
+ * copies" (section "Practice"): a two-stage copy-and-reduce over the rows of
+ * X (rows x cols fp32, row-major, cols a multiple of 4, at most 8192).  One
+ * producer thread per block copies row perm[r] into stage (t % 2) with a bulk
+ * copy; four consumer warps each sum a quarter of the stage and atomically add
+ * it to out[r] (the caller zeroes out; rows r = block, block + grid, ...).
+ * check_reuse != 0: the producer waits until every consumer warp has finished
+ * the tile that last used a stage before overwriting it (the consume-before-
+ * reuse edge).  check_reuse == 0: that one wait is skipped.  delay_warp (0..3,
+ * or -1 for none) sleeps delay_ns before reading each tile.  trace (device,
+ * may be NULL): trace[0] counts events of block 0, then up to trace_cap pairs
+ * {globaltimer ns, event << 56 | stage << 48 | warp << 40 | tile}; events 1
+ * load issued, 2 load landed, 3 reuse wait begins, 4 reuse allowed, 5 read
+ * begins, 6 read ends.  All pointers are device pointers; asynchronous on
+ * `stream`; every wait is bounded (see pgemm_get_device_status). */
+PGEMM_API pgemm_status pgemm_stage_reuse_demo(const float *X, int rows, int cols, const int *perm,
+                                              float *out, int check_reuse, int delay_warp,
+                                              unsigned delay_ns, unsigned long long *trace,
+                                              int trace_cap, pgemm_stream_t stream);
+
 /* Synchronises `stream`, then reads and clears the library's device status
  * word of the current device: PGEMM_OK, or PGEMM_ERR_TIMEOUT if a kernel's
  * bounded mbarrier wait ran out (the kernel then skipped the rest of its work

@@ -20,6 +20,7 @@ __all__ = [
     "gemm_bf16_ex", "gemm_i8_ex", "pgemm_default_config", "pgemm_list_configs",
     "pgemm_kernel_attrs", "pgemm_get_device_status", "pgemm_selftest_wait_timeout",
     "pgemm_status_string", "pgemm_version", "gemm_i8_noalloc", "NOALLOC_SCRATCH_BYTES",
+    "pgemm_stage_reuse_demo",
     "DTYPES", "STATUS", "EXPORTED",
 ]
 
@@ -39,7 +40,7 @@ EXPORTED = [
     "gemm_f32", "gemm_bf16", "gemm_i8", "gemm_f32_ex", "gemm_bf16_ex", "gemm_i8_ex",
     "pgemm_default_config", "pgemm_list_configs", "pgemm_kernel_attrs",
     "pgemm_get_device_status", "pgemm_selftest_wait_timeout", "pgemm_status_string",
-    "pgemm_version", "gemm_i8_noalloc",
+    "pgemm_version", "gemm_i8_noalloc", "pgemm_stage_reuse_demo",
 ]
 
 
@@ -82,6 +83,7 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
         "pgemm_selftest_wait_timeout": [i, vp],
         "pgemm_status_string": [i],
         "pgemm_version": [],
+        "pgemm_stage_reuse_demo": [vp, i, i, vp, vp, i, i, ctypes.c_uint, vp, i, vp],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -188,6 +190,17 @@ def gemm_bf16_ex(M, N, K, alpha, A, B, beta, C, config=None, stream=None):
 def gemm_i8_ex(M, N, K, alpha, A, B, beta, C, config=None, stream=None):
     _check(lib().gemm_i8_ex(M, N, K, int(alpha), _ptr(A), _ptr(B), int(beta), _ptr(C),
                             _cfg(config), _stream(stream)), "gemm_i8_ex")
+
+
+def pgemm_stage_reuse_demo(X, rows, cols, perm, out, check_reuse, delay_warp=-1, delay_ns=0,
+                           trace=None, trace_cap=0, stream=None):
+    """The two-stage copy-and-reduce hazard experiment (with or without the
+    consume-before-reuse wait).  X: rows x cols fp32, perm: int32 row order,
+    out: rows fp32 (zeroed by the caller); trace: optional uint64 buffer."""
+    _check(lib().pgemm_stage_reuse_demo(_ptr(X), rows, cols, _ptr(perm), _ptr(out),
+                                        int(check_reuse), int(delay_warp), int(delay_ns),
+                                        _ptr(trace), int(trace_cap), _stream(stream)),
+           "pgemm_stage_reuse_demo")
 
 
 def pgemm_default_config(dtype: str, M: int, N: int, K: int):

@@ -492,6 +492,29 @@ pgemm_status pgemm_selftest_wait_timeout(int limit_us, pgemm_stream_t stream) {
     return pgemm_get_device_status(stream);
 }
 
+pgemm_status pgemm_stage_reuse_demo(const float *X, int rows, int cols, const int *perm,
+                                    float *out, int check_reuse, int delay_warp,
+                                    unsigned delay_ns, unsigned long long *trace, int trace_cap,
+                                    pgemm_stream_t stream) {
+    if (rows < 0 || cols <= 0 || cols % 4 != 0 || cols > 8192 || trace_cap < 0 ||
+        delay_warp < -1 || delay_warp > 3)
+        return PGEMM_ERR_INVALID_VALUE;
+    if (rows == 0) return PGEMM_OK;
+    if (!X || !perm || !out) return PGEMM_ERR_INVALID_VALUE;
+    if (!aligned16(X)) return PGEMM_ERR_MISALIGNED;
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    DeviceState *d = nullptr;
+    pgemm_status st = device_setup(&dev, &d);
+    if (st != PGEMM_OK) return st;
+    KernelCtx ctx{d->status, kDefaultWaitLimitNs};
+    const int blocks = rows < d->sm_count ? rows : d->sm_count;
+    return launch_stage_reuse(X, rows, cols, perm, out, check_reuse, delay_warp, delay_ns, trace,
+                              trace_cap, blocks, ctx, stream) == cudaSuccess
+               ? PGEMM_OK
+               : PGEMM_ERR_CUDA;
+}
+
 const char *pgemm_status_string(pgemm_status status) {
     switch (status) {
         case PGEMM_OK: return "ok";

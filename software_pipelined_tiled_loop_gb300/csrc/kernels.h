@@ -85,3 +85,11 @@ pgemm_status gemm_i8_fixed_scratch(int M, int N, int K, int32_t alpha, const int
                                    const int8_t *B, int32_t beta, int32_t *C, void *scratch,
                                    long long scratch_bytes, cudaStream_t stream);
 }  // namespace pg
+
+namespace pg {
+// stage_reuse.cu: the two-stage copy-and-reduce hazard experiment.
+cudaError_t launch_stage_reuse(const float *X, int rows, int cols, const int *perm, float *out,
+                               int check_reuse, int delay_warp, unsigned delay_ns,
+                               unsigned long long *trace_buf, int trace_cap, int blocks,
+                               KernelCtx ctx, cudaStream_t stream);
+}  // namespace pg

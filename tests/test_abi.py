@@ -93,3 +93,13 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(pg, "_lib", None)
     with pytest.raises(RuntimeError):
         pg.lib()
+
+
+def test_stage_reuse_demo_validation_without_gpu(L):
+    good = 1 << 20
+    f = L.pgemm_stage_reuse_demo
+    assert f(good, 4, 3, good, good, 1, -1, 0, None, 0, None) == 1      # cols % 4
+    assert f(good, 4, 16384, good, good, 1, -1, 0, None, 0, None) == 1  # too wide for 2 stages
+    assert f(good, 4, 16, good, good, 1, 7, 0, None, 0, None) == 1      # no such warp
+    assert f(good + 4, 4, 16, good, good, 1, -1, 0, None, 0, None) == 2  # misaligned X
+    assert f(good, 0, 16, None, None, 1, -1, 0, None, 0, None) == 0      # nothing to do
