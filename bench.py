@@ -601,7 +601,7 @@ def main():
             "ms_per_step": round(main_res["ms_per_step"], 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None,
             "dtype": {"f32": "f32", "bf16": "bf16", "i8": "int8"}[dtype],
-            "data": "synthetic (seeded; see DESIGN.md input recipe)",
+            "data": "synthetic (seeded splitmix64 draws; recipes in seeded_inputs.workload)",
             "config": {**config, "tile_stages": main_res["config"],
                        "parallelism": "replicas" if ctx.world > 1 else "single"},
             "roofline": roof,

@@ -123,12 +123,14 @@ static const KernelInfo *table_of(pgemm_dtype dt, int *count) {
 //  * fp32: 128 x 128 tiles with three stages (two blocks per SM; four or more
 //    stages drop to one block per SM and lose 16 %); 128 x 64 tiles when the
 //    128 x 128 grid would leave SMs without two blocks each.
-//  * bf16 / int8: 128 x 256 tiles with four stages (the deepest ring that fits)
-//    when those tiles cover every SM, else 128 x 128 with four; shapes whose
-//    rows are not 16-byte aligned use the two-CTA 256 x 256 cluster tiles
-//    (measured 14 % faster on 4095 x 4097 x 4100).
+//  * bf16: 256 x 256 tiles on a CTA pair (cta_group::2) with six stages when
+//    the pairs cover the GPU (12 % over 128 x 256 on 8192^3); else 128 x 256
+//    with four stages when those tiles cover every SM; else 128 x 128.
+//  * int8: 128 x 256 with four stages (the pair is slower here: its
+//    256-product rounds synchronise both CTAs' epilogues); else 128 x 128.
 static pgemm_config default_config(pgemm_dtype dt, int M, int N, int K, int sm_count) {
-    pgemm_config c{128, 128, 0, 0};
+    (void)K;
+    pgemm_config c{128, 128, 0, 4};
     if (dt == PGEMM_F32) {
         const long long tiles128 = (long long)((M + 127) / 128) * ((N + 127) / 128);
         c.bn = tiles128 >= 2LL * sm_count ? 128 : 64;
@@ -136,17 +138,14 @@ static pgemm_config default_config(pgemm_dtype dt, int M, int N, int K, int sm_c
         return c;
     }
     const long long tiles256 = (long long)((M + 127) / 128) * ((N + 255) / 256);
-    const int elem = dt == PGEMM_BF16 ? 2 : 1;
-    const bool misaligned = (static_cast<long long>(K) * elem) % 16 != 0 ||
-                            (static_cast<long long>(N) * elem) % 16 != 0 ||
-                            (static_cast<long long>(N) * 4) % 16 != 0;
-    if (tiles256 >= sm_count) {
-        c.bm = misaligned && M > 128 ? 256 : 128;
+    const long long pairs = (long long)((M + 255) / 256) * ((N + 255) / 256);
+    if (dt == PGEMM_BF16 && pairs >= sm_count / 2) {
+        c.bm = 256;
         c.bn = 256;
-    } else {
-        c.bn = 128;
+        c.stages = 6;
+    } else if (tiles256 >= sm_count) {
+        c.bn = 256;
     }
-    c.stages = 4;
     return c;
 }
 

@@ -8,10 +8,11 @@ namespace pg {
 // 256-wide tiles use eight epilogue warps (two per TMEM lane quadrant), so a
 // tile's epilogue takes half as long; 128-wide tiles keep four, which leaves
 // room for two resident blocks per SM at shallow rings.
-// CM = 2: two CTAs of a cluster compute a 256 x BN tile and share its B panel
-// (TMA multicast), listed as bm = 256.
+// CM = CG = 2: a CTA pair computes a 256 x BN tile with one M = 256 MMA (each
+// CTA holds half of A's rows and half of B's columns), listed as bm = 256.
 template <int BN, int STAGES, int CM = 1>
-using Bf16Cfg = TcCfg<BN, STAGES, /*KC=*/0, /*BF16=*/1, /*INT_FOLD=*/false, BN == 256 ? 8 : 4, CM>;
+using Bf16Cfg =
+    TcCfg<BN, STAGES, /*KC=*/0, /*BF16=*/1, /*INT_FOLD=*/false, BN == 256 ? 8 : 4, CM, CM>;
 
 template <int BN, int STAGES, int CM = 1>
 static KernelInfo info_bf16() {
@@ -28,7 +29,7 @@ const KernelInfo *bf16_kernels(int *count) {
         // S = 1: one slot, load and compute strictly alternate (the unpipelined
         // comparator: "kernel 10" of the SGEMM page)
         info_bf16<256, 1>(), info_bf16<128, 1>(),
-        info_bf16<256, 3, 2>(), info_bf16<256, 4, 2>(),
+        info_bf16<256, 4, 2>(), info_bf16<256, 5, 2>(), info_bf16<256, 6, 2>(),
     };
     *count = static_cast<int>(sizeof(table) / sizeof(table[0]));
     return table;

@@ -24,7 +24,8 @@ constexpr int kI8ChunkTiles = 4;  // 4 K-tiles of 64 = 256 products per exact fp
 // Each epilogue thread keeps a 128-column row of int32 sums in registers:
 // 128-wide tiles use four epilogue warps, 256-wide tiles eight.
 template <int BN, int STAGES, int CM = 1>
-using I8Cfg = TcCfg<BN, STAGES, kI8ChunkTiles, /*BF16=*/0, /*INT_FOLD=*/true, BN == 256 ? 8 : 4, CM>;
+using I8Cfg =
+    TcCfg<BN, STAGES, kI8ChunkTiles, /*BF16=*/0, /*INT_FOLD=*/true, BN == 256 ? 8 : 4, CM, CM>;
 
 template <int BN, int STAGES, int CM = 1>
 static KernelInfo info_i8() {
@@ -38,7 +39,7 @@ const KernelInfo *i8_kernels(int *count) {
         info_i8<256, 1>(), info_i8<256, 2>(), info_i8<256, 3>(), info_i8<256, 4>(),
         info_i8<128, 2>(), info_i8<128, 3>(), info_i8<128, 4>(), info_i8<128, 5>(),
         info_i8<128, 6>(), info_i8<128, 1>(),
-        info_i8<256, 3, 2>(), info_i8<256, 4, 2>(),
+        info_i8<256, 4, 2>(), info_i8<256, 5, 2>(), info_i8<256, 6, 2>(),
     };
     *count = static_cast<int>(sizeof(table) / sizeof(table[0]));
     return table;

@@ -57,20 +57,26 @@ namespace pg {
 // all of K); BF16: operand type (1 = bf16, 0 = fp16); INT_FOLD: exact-int8
 // epilogue (fold fp32 chunk sums into int32 registers); EPI: epilogue warps
 // (4: one per TMEM lane quadrant; 8: two per quadrant, each half the columns).
-// CM: CTAs per cluster along M (1, or 2: the pair computes two vertically
-// adjacent tiles and shares one B panel, each CTA loading half of it by TMA
-// multicast into both CTAs' shared memory).
-template <int BN_, int STAGES_, int KC_, int BF16_, bool INT_FOLD_, int EPI_ = 4, int CM_ = 1>
+// CM: CTAs per cluster along M, CG: tcgen05 CTA group; either both 1, or both
+// 2: a CTA pair computes a 256 x BN tile with one M = 256 MMA issued by the
+// even CTA; each CTA loads and holds its 128 rows of A and half of B's
+// columns (so a stage is a third smaller and the ring one to two stages
+// deeper), and receives its 128 rows of the accumulator in its own TMEM.
+template <int BN_, int STAGES_, int KC_, int BF16_, bool INT_FOLD_, int EPI_ = 4, int CM_ = 1,
+          int CG_ = 1>
 struct TcCfg {
     static constexpr int BM = 128, BN = BN_, BK = 64, STAGES = STAGES_, KC = KC_, CM = CM_;
+    static constexpr int CG = CG_;
+    static constexpr int B_COLS = BN / CG;  // B columns this CTA loads and holds
     static constexpr int BF16 = BF16_;
     static constexpr bool INT_FOLD = INT_FOLD_;
     static constexpr int EPI = EPI_;
     static constexpr int EPI_COLS = BN * 4 / EPI;  // columns per epilogue warp
     using Scalar = typename std::conditional<INT_FOLD, int32_t, float>::type;
     static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = BN * BK * 2;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int B_BYTES = B_COLS * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // per CTA
+    static constexpr int TX_BYTES = STAGE_BYTES * CG;      // counted on the MMA's full barrier
     static constexpr int STAGING_BYTES = EPI * 32 * 32 * 4;  // one 32x32 block per warp
     static constexpr int ACC_COLS = BN;        // fp32 accumulator: one TMEM column per n
     static constexpr int TMEM_COLS = 2 * BN;   // two accumulators
@@ -89,7 +95,8 @@ struct TcCfg {
     static_assert(EPI_COLS % 32 == 0, "epilogue column split");
     static_assert(!INT_FOLD || EPI_COLS == 128, "the int32 fold keeps 128 columns per thread");
     static_assert(USED + 1024 <= 232448, "shared memory");
-    static_assert(CM == 1 || (CM == 2 && (BN / 64) % 2 == 0), "cluster split of B");
+    static_assert((CM == 1 && CG == 1) || (CM == 2 && CG == 2 && (BN / 64) % 2 == 0),
+                  "a CTA pair is a cluster of two splitting B's columns in halves");
 };
 
 // One warp writes a 32 x 32 block of C: rows [m_base, m_base + 32), columns
@@ -153,6 +160,16 @@ __device__ __forceinline__ void store_block32(const GemmArgs<Scalar, Scalar> &a,
     }
 }
 
+// Hand an accumulator back to the MMA issuer: a local arrive, or with a CTA
+// pair an arrive on the even CTA's barrier (remote from the odd CTA).
+template <class Cfg>
+__device__ __forceinline__ void release_acc(uint64_t *acc_empty_bar) {
+    if constexpr (Cfg::CG == 2)
+        mbar_arrive_cluster(mapa_shared(smem_u32(acc_empty_bar), 0));
+    else
+        mbar_arrive(acc_empty_bar);
+}
+
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
@@ -183,31 +200,38 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         if (args.c_tma) prefetch_tmap(&tmap_c);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
-            // released by the MMA issuer of every CTA whose B half lands here
-            mbar_init(&empty[s], Cfg::CM);
+            // released by the MMA issuer (with a CTA pair: the even CTA's, whose
+            // MMAs read this CTA's stage too)
+            mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
-            mbar_init(&acc_empty[b], Cfg::EPI);
+            // with a CTA pair the even CTA's barrier counts both CTAs' epilogues
+            mbar_init(&acc_empty[b], Cfg::EPI * Cfg::CG);
         }
         mbar_init(mma_done, 1);
         fence_barrier_init();
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
-        tmem_relinquish();
+        if constexpr (Cfg::CG == 2) {
+            tmem_alloc_pair(tmem_slot, Cfg::TMEM_COLS);  // both CTAs; same address in each
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncwarp();
     if constexpr (Cfg::CM > 1)
-        cluster_sync();  // the peer's barriers exist before any multicast reaches them
+        cluster_sync();  // the peer's barriers exist before anything reaches them
     else
         __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    // Cluster geometry: with CM > 1 a "tile" of the schedule is a CM x 1 stack
-    // of output tiles; this CTA computes the one at its cluster rank.
+    // Cluster geometry: with a CTA pair a "tile" of the schedule is a 2 x 1
+    // stack of 128-row tiles; this CTA computes the one at its cluster rank.
     const uint32_t crank = Cfg::CM > 1 ? cluster_ctarank() : 0u;
     const int sched_id = static_cast<int>(blockIdx.x) / Cfg::CM;
     const int sched_stride = static_cast<int>(gridDim.x) / Cfg::CM;
@@ -234,29 +258,32 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         ok = false;
                         break;
                     }
+                    if constexpr (Cfg::CG == 2) {
+                        // Both CTAs load their A rows and B columns into their own
+                        // shared memory; the bytes are counted on the even CTA's
+                        // full barrier, which its producer arms for both.
+                        const uint32_t full_lead = mapa_shared(smem_u32(&full[s]), 0);
+                        if (crank == 0) mbar_arrive_expect_tx(&full[s], Cfg::TX_BYTES);
+                        tma_load_2d_pair(sA + s * Cfg::A_BYTES, &tmap_a, full_lead, kt * BK, m0);
+#pragma unroll
+                        for (int j = 0; j < Cfg::B_COLS / 64; ++j)
+                            tma_load_2d_pair(sB + s * Cfg::B_BYTES + j * (BK * 128), &tmap_b,
+                                             full_lead,
+                                             n0 + static_cast<int>(crank) * Cfg::B_COLS + j * 64,
+                                             kt * BK);
+                        continue;
+                    }
                     mbar_arrive_expect_tx(&full[s], Cfg::STAGE_BYTES);
                     tma_load_2d(sA + s * Cfg::A_BYTES, &tmap_a, &full[s], kt * BK, m0);
-                    if constexpr (Cfg::CM == 1) {
 #pragma unroll
-                        for (int j = 0; j < BN / 64; ++j)
-                            tma_load_2d(sB + s * Cfg::B_BYTES + j * (BK * 128), &tmap_b, &full[s],
-                                        n0 + j * 64, kt * BK);
-                    } else {
-                        // this CTA's share of the B boxes, written into every CTA of the pair
-                        constexpr int JB = BN / 64 / Cfg::CM;
-#pragma unroll
-                        for (int jj = 0; jj < JB; ++jj) {
-                            const int j = static_cast<int>(crank) * JB + jj;
-                            tma_load_2d_multicast(sB + s * Cfg::B_BYTES + j * (BK * 128), &tmap_b,
-                                                  &full[s], n0 + j * 64, kt * BK,
-                                                  static_cast<uint16_t>((1u << Cfg::CM) - 1u));
-                        }
-                    }
+                    for (int j = 0; j < BN / 64; ++j)
+                        tma_load_2d(sB + s * Cfg::B_BYTES + j * (BK * 128), &tmap_b, &full[s],
+                                    n0 + j * 64, kt * BK);
                 }
             }
             if constexpr (Cfg::CM > 1) {
-                // Producer tail: wait for the last release of every stage.  That
-                // includes the peer MMA issuer's multicast arrivals on this CTA's
+                // Producer tail: wait for the last release of every stage.  Those
+                // are the pair MMA issuer's multicast arrivals on this CTA's
                 // barriers, so none can land after the cluster has been left.
                 for (int i = 0; ok && i < STAGES; ++i, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
@@ -265,10 +292,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
+        // with a CTA pair only the even CTA issues (its MMAs cover both CTAs)
+        if (lane == 0 && (Cfg::CG == 1 || crank == 0)) {
             // ---------------- MMA issuer ----------------
-            constexpr uint32_t idesc = idesc_f16(BM, BN, Cfg::BF16, /*A K-major*/ 0,
+            constexpr uint32_t idesc = idesc_f16(BM * Cfg::CG, BN, Cfg::BF16, /*A K-major*/ 0,
                                                  /*B N-major*/ 1);
+            constexpr uint16_t kPair = 3;  // both CTAs of the pair
             uint32_t it = 0, gr = 0;
             bool ok = true;
             for (int tile = sched_id; ok && tile < num_tiles; tile += sched_stride) {
@@ -295,19 +324,31 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         for (int k = 0; k < BK / 16; ++k) {
                             const uint64_t ad = smem_desc_sw128(a_addr + k * 32, 16, 1024);
                             const uint64_t bd = smem_desc_sw128(b_addr + k * 2048, BK * 128, 1024);
-                            umma_f16_ss(d_tmem, ad, bd, idesc, (first && k == 0) ? 0u : 1u);
+                            if constexpr (Cfg::CG == 2)
+                                umma_f16_ss_pair(d_tmem, ad, bd, idesc, (first && k == 0) ? 0u : 1u);
+                            else
+                                umma_f16_ss(d_tmem, ad, bd, idesc, (first && k == 0) ? 0u : 1u);
                         }
-                        // stage s is free once these MMAs have read it (in every CTA whose
-                        // producer wrote into it)
-                        if constexpr (Cfg::CM == 1)
-                            umma_commit(&empty[s]);
+                        // stage s is free once these MMAs have read it (in both CTAs
+                        // of a pair)
+                        if constexpr (Cfg::CG == 2)
+                            umma_commit_pair_multicast(&empty[s], kPair);
                         else
-                            umma_commit_multicast(&empty[s], static_cast<uint16_t>((1u << Cfg::CM) - 1u));
+                            umma_commit(&empty[s]);
                     }
-                    if (ok) umma_commit(&acc_full[ab]);  // round complete -> epilogue
+                    // round complete -> epilogue (of both CTAs, with a pair)
+                    if (ok) {
+                        if constexpr (Cfg::CG == 2)
+                            umma_commit_pair_multicast(&acc_full[ab], kPair);
+                        else
+                            umma_commit(&acc_full[ab]);
+                    }
                 }
             }
-            umma_commit(mma_done);
+            if constexpr (Cfg::CG == 2)
+                umma_commit_pair_multicast(mma_done, 1);  // this CTA's barrier only
+            else
+                umma_commit(mma_done);
             mbar_wait(mma_done, 0, ctx, kSiteMmaDone);
         }
     } else {
@@ -355,7 +396,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     }
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&acc_empty[ab]);
+                    if (lane == 0) release_acc<Cfg>(&acc_empty[ab]);
                 }
                 if (!ok) break;
                 const uint32_t bias = static_cast<uint32_t>(rounds) * 0x4B400000u;  // mod 2^32
@@ -383,7 +424,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                             // last TMEM read of this accumulator: hand it back
                             tc_fence_before();
                             __syncwarp();
-                            if (lane == 0) mbar_arrive(&acc_empty[ab]);
+                            if (lane == 0) release_acc<Cfg>(&acc_empty[ab]);
                         }
                         if (in_range)
                             store_block32(args, &tmap_c, buf, m_base, n0 + col0 + c, v, true,
@@ -410,13 +451,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     tc_fence_before();
     __syncwarp();
     if constexpr (Cfg::CM > 1)
-        cluster_sync();  // no CTA leaves while its peer may still write into it
+        cluster_sync();  // no CTA leaves while its peer may still signal it
     else
         __syncthreads();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+        if constexpr (Cfg::CG == 2)
+            tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+        else
+            tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
     }
 }
 

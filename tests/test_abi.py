@@ -56,7 +56,9 @@ def test_list_configs(L):
     for cfgs in (f32, bf16, i8):
         assert {c[3] for c in cfgs} == {1, 2, 3, 4, 5, 6}
     assert {c[3] for c in bf16 if c[1] == 128} == {1, 2, 3, 4, 5, 6}
-    assert {c[3] for c in bf16 if c[1] == 256} == {1, 2, 3, 4}
+    # 128 x 256 single-CTA tiles fit four stages; the CTA pair's 256 x 256 six
+    assert {c[3] for c in bf16 if c[1] == 256 and c[0] == 128} == {1, 2, 3, 4}
+    assert {c[3] for c in bf16 if c[0] == 256} == {4, 5, 6}
 
 
 @pytest.mark.parametrize("fn", ["gemm_f32", "gemm_bf16", "gemm_i8"])
