@@ -96,7 +96,7 @@ PGEMM_API pgemm_status gemm_bf16(int M, int N, int K, float alpha, const uint16_
  * into int32; C <- alpha*acc + beta*C in int32 arithmetic modulo 2^32 (two's
  * complement wrap-around).  The products run on the tensor cores as fp16
  * values (exact for |v| <= 128) with exact fp32 partial sums over K chunks of
- * at most 256, folded into int32. */
+ * at most 1024, folded into int32. */
 PGEMM_API pgemm_status gemm_i8(int M, int N, int K, int32_t alpha, const int8_t *A, const int8_t *B,
                      int32_t beta, int32_t *C, pgemm_stream_t stream);
 

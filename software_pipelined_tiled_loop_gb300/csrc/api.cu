@@ -123,11 +123,10 @@ static const KernelInfo *table_of(pgemm_dtype dt, int *count) {
 //  * fp32: 128 x 128 tiles with three stages (two blocks per SM; four or more
 //    stages drop to one block per SM and lose 16 %); 128 x 64 tiles when the
 //    128 x 128 grid would leave SMs without two blocks each.
-//  * bf16: 256 x 256 tiles on a CTA pair (cta_group::2) with six stages when
-//    the pairs cover the GPU (12 % over 128 x 256 on 8192^3); else 128 x 256
-//    with four stages when those tiles cover every SM; else 128 x 128.
-//  * int8: 128 x 256 with four stages (the pair is slower here: its
-//    256-product rounds synchronise both CTAs' epilogues); else 128 x 128.
+//  * bf16 and int8: 256 x 256 tiles on a CTA pair (cta_group::2) with six
+//    stages when the pairs cover the GPU (bf16 8192^3 +12 %, int8 4096^3
+//    +10 % over 128 x 256); else 128 x 256 with four stages when those tiles
+//    cover every SM; else 128 x 128.
 static pgemm_config default_config(pgemm_dtype dt, int M, int N, int K, int sm_count) {
     (void)K;
     pgemm_config c{128, 128, 0, 4};
@@ -139,7 +138,7 @@ static pgemm_config default_config(pgemm_dtype dt, int M, int N, int K, int sm_c
     }
     const long long tiles256 = (long long)((M + 127) / 128) * ((N + 255) / 256);
     const long long pairs = (long long)((M + 255) / 256) * ((N + 255) / 256);
-    if (dt == PGEMM_BF16 && pairs >= sm_count / 2) {
+    if (pairs >= sm_count / 2) {
         c.bm = 256;
         c.bn = 256;
         c.stages = 6;

@@ -2,12 +2,12 @@
 //
 // sm_103a has no integer tcgen05.mma kind, so the int8 products run as fp16
 // products: every int8 value is exact in fp16 (|v| <= 128 < 2^11), every
-// product is exact in fp32 (|a*b| <= 2^14), and a sum of at most KC*64 = 256
-// such products stays an integer of magnitude <= 2^22, exact in fp32.  The
-// tensor core therefore accumulates each K-chunk of 256 exactly in TMEM, and
-// the epilogue warps convert each chunk to int32 and add it into registers
-// (int32 arithmetic modulo 2^32), finally writing alpha*acc + beta*C modulo
-// 2^32.  Bit-exact against the int64 oracle.
+// product is exact in fp32 (|a*b| <= 2^14), and a sum of at most KC*64 = 1024
+// such products is an integer of magnitude <= 2^24, which fp32 represents
+// exactly.  The tensor core therefore accumulates each K-round of 1024
+// exactly in TMEM, and the epilogue warps convert each round to int32 and add
+// it into registers (int32 arithmetic modulo 2^32), finally writing
+// alpha*acc + beta*C modulo 2^32.  Bit-exact against the int64 oracle.
 //
 // The widening int8 -> fp16 is a separate, HBM-bound pass over A and B into
 // stream-ordered scratch (rows padded to 16-byte pitches for TMA); widening
@@ -19,7 +19,7 @@
 
 namespace pg {
 
-constexpr int kI8ChunkTiles = 4;  // 4 K-tiles of 64 = 256 products per exact fp32 round
+constexpr int kI8ChunkTiles = 16;  // 16 K-tiles of 64 = 1024 products per exact fp32 round
 
 // Each epilogue thread keeps a 128-column row of int32 sums in registers:
 // 128-wide tiles use four epilogue warps, 256-wide tiles eight.

@@ -25,8 +25,8 @@
 //
 // An accumulation round is the whole K range of an output tile (bf16), or a
 // chunk of KC K-tiles (exact int8: a chunk's fp32 partial sums of fp16
-// products of int8 values stay integers below 2^24 and are exact; the
-// epilogue converts each chunk to int32 and adds it into registers).
+// products of int8 values stay integers of magnitude <= 2^24 and are exact;
+// the epilogue converts each chunk to int32 and adds it into registers).
 //
 // The kernel is persistent (grid = resident blocks, output tiles strided by
 // the grid) and TMEM holds two accumulators, so the epilogue of one round
@@ -94,6 +94,7 @@ struct TcCfg {
     static_assert(EPI == 4 || EPI == 8, "EPI");
     static_assert(EPI_COLS % 32 == 0, "epilogue column split");
     static_assert(!INT_FOLD || EPI_COLS == 128, "the int32 fold keeps 128 columns per thread");
+    static_assert(!INT_FOLD || KC * BK <= 1024, "a round's fp32 sum must stay below 2^24");
     static_assert(USED + 1024 <= 232448, "shared memory");
     static_assert((CM == 1 && CG == 1) || (CM == 2 && CG == 2 && (BN / 64) % 2 == 0),
                   "a CTA pair is a cluster of two splitting B's columns in halves");
@@ -367,11 +368,15 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             const bool in_range = m0 < args.M;  // the second tile of a pair may lie below C
             const int m_base = m0 + static_cast<int>(q * 32);
             if constexpr (Cfg::INT_FOLD) {
-                // Exact int8: sum the chunks' integer-valued fp32 partials in
-                // int32.  For an integer-valued x with |x| <= 2^22, x + 1.5*2^23
-                // is exact and its bit pattern is 0x4B400000 + x, so each value
-                // costs one FADD and one IADD (no quarter-rate F2I); the
-                // 0x4B400000 of every round is subtracted once at the end.
+                // Exact int8: sum the rounds' integer-valued fp32 partials in
+                // int32.  Rounds of at most 256 products (|x| <= 2^22) convert
+                // with one FADD: for an integer-valued x with |x| <= 2^22,
+                // x + 1.5*2^23 is exact and its bit pattern is 0x4B400000 + x
+                // (the 0x4B400000 of every round is subtracted once at the
+                // end).  Longer rounds (up to 1024 products, |x| <= 2^24) use
+                // the exact float-to-int conversion, which is slower per value
+                // but needed 4x less often.
+                constexpr bool kMagicFold = Cfg::KC * Cfg::BK <= 256;
                 constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
                 uint32_t acc[Cfg::EPI_COLS];
 #pragma unroll
@@ -391,15 +396,20 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         tmem_ld_32x32b_x16(t_row + c, v);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            acc[c + j] += __float_as_uint(__uint_as_float(v[j]) + kMagic);
+                        for (int j = 0; j < 16; ++j) {
+                            if constexpr (kMagicFold)
+                                acc[c + j] += __float_as_uint(__uint_as_float(v[j]) + kMagic);
+                            else
+                                acc[c + j] += static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[j])));
+                        }
                     }
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) release_acc<Cfg>(&acc_empty[ab]);
                 }
                 if (!ok) break;
-                const uint32_t bias = static_cast<uint32_t>(rounds) * 0x4B400000u;  // mod 2^32
+                const uint32_t bias =
+                    kMagicFold ? static_cast<uint32_t>(rounds) * 0x4B400000u : 0u;  // mod 2^32
 #pragma unroll
                 for (int j = 0; j < Cfg::EPI_COLS; ++j) acc[j] -= bias;
                 if (in_range) {

@@ -150,7 +150,7 @@ def test_persistent_multi_tile_per_block(orc, dtype):
 
 
 # -------------------------------------------------------------- int8 exact ----
-@pytest.mark.parametrize("K", [1, 255, 256, 257, 1024, 4096])
+@pytest.mark.parametrize("K", [1, 255, 256, 257, 1023, 1024, 1025, 2049, 4096])
 def test_int8_extremes_bit_exact(orc, K):
     M, N = 130, 136
     for a, b in ((-128, -128), (127, 127), (-128, 127)):
