@@ -175,31 +175,58 @@ static pgemm_status encode_2d(CUtensorMap *map, CUtensorMapDataType type, int el
 }
 
 // Copies rows [0, rows) x [0, cols) of a row-major matrix with pitch `sld` to a
-// new pitch `dld` (both in elements of `eb` bytes).
-__global__ void repack_rows_kernel(const uint8_t *__restrict__ src, long long sld,
-                                   uint8_t *__restrict__ dst, long long dld, int rows, int cols,
-                                   int eb) {
-    const long long total = static_cast<long long>(rows) * cols;
-    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
-         i += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const long long r = i / cols, c = i - r * cols;
-        const uint8_t *s = src + (r * sld + c) * eb;
-        uint8_t *d = dst + (r * dld + c) * eb;
-        if (eb == 2)
-            *reinterpret_cast<uint16_t *>(d) = *reinterpret_cast<const uint16_t *>(s);
-        else
-            *reinterpret_cast<uint32_t *>(d) = *reinterpret_cast<const uint32_t *>(s);
+// new pitch `dld` (both in elements of `eb` bytes, 2 or 4; the destination rows
+// start on 16-byte boundaries).  One block walks a row at a time; every
+// 16-byte destination chunk is assembled from the one or two aligned 16-byte
+// source chunks that cover it (a byte shift by the row's misalignment, which
+// is even), so every store is a full 16-byte vector.  A chunk whose source
+// window would reach past the end of the source matrix is copied in 2-byte
+// units instead, as is the row's tail shorter than 16 bytes.
+__device__ __forceinline__ uint4 shift_bytes(uint4 lo, uint4 hi, uint32_t off) {
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    const uint32_t q = off >> 2, sh = (off & 3u) * 8u;  // sh is 0 or 16: offsets are even
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t a = w[(q + i) & 7], b = w[(q + i + 1) & 7];
+        o[i] = sh ? __funnelshift_r(a, b, sh) : a;
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__global__ void repack_rows_kernel(const uint8_t *__restrict__ src, long long sld, uint8_t *__restrict__ dst,
+                                   long long dld, int rows, int cols, int eb) {
+    const long long row_bytes = static_cast<long long>(cols) * eb;
+    const uint8_t *src_end = src + (static_cast<long long>(rows - 1) * sld + cols) * eb;
+    for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+        const uint8_t *s = src + static_cast<long long>(r) * sld * eb;
+        uint8_t *d = dst + static_cast<long long>(r) * dld * eb;
+        const uint32_t off = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(s) & 15u);
+        const uint4 *sa = reinterpret_cast<const uint4 *>(s - off);  // aligned down
+        const long long nchunks = row_bytes / 16;
+        for (long long j = threadIdx.x; j < nchunks; j += blockDim.x) {
+            const uint8_t *win_end = reinterpret_cast<const uint8_t *>(sa + j) + (off ? 32 : 16);
+            if (win_end <= src_end) {
+                const uint4 lo = sa[j];
+                reinterpret_cast<uint4 *>(d)[j] = off ? shift_bytes(lo, sa[j + 1], off) : lo;
+            } else {
+#pragma unroll
+                for (int b = 0; b < 16; b += 2)
+                    *reinterpret_cast<uint16_t *>(d + 16 * j + b) =
+                        *reinterpret_cast<const uint16_t *>(s + 16 * j + b);
+            }
+        }
+        for (long long b = nchunks * 16 + 2 * threadIdx.x; b < row_bytes; b += 2 * blockDim.x)
+            *reinterpret_cast<uint16_t *>(d + b) = *reinterpret_cast<const uint16_t *>(s + b);
     }
 }
 
 static cudaError_t launch_repack(const void *src, long long sld, void *dst, long long dld,
                                  int rows, int cols, int eb, int sm_count, cudaStream_t s) {
-    const long long total = static_cast<long long>(rows) * cols;
-    if (total <= 0) return cudaSuccess;
-    long long blocks = (total + 255) / 256;
-    if (blocks > static_cast<long long>(sm_count) * 8) blocks = static_cast<long long>(sm_count) * 8;
-    repack_rows_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(
-        static_cast<const uint8_t *>(src), sld, static_cast<uint8_t *>(dst), dld, rows, cols, eb);
+    if (rows <= 0 || cols <= 0) return cudaSuccess;
+    const int blocks = rows < sm_count * 8 ? rows : sm_count * 8;
+    repack_rows_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint8_t *>(src), sld,
+                                              static_cast<uint8_t *>(dst), dld, rows, cols, eb);
     return cudaGetLastError();
 }
 

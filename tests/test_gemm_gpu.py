@@ -69,7 +69,7 @@ def check(orc, dtype, M, N, K, alpha, beta, seed, kind="random", config=None):
 
 # ---------------------------------------------------------------- basics ----
 @pytest.mark.parametrize("dtype", ["bf16", "f32", "i8"])
-@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (1, 1, 1), (300, 520, 200), (257, 129, 1000),
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (1, 1, 1), (300, 520, 200), (257, 129, 1000), (67, 77, 131), (33, 1001, 70),
                                    (64, 1000, 96), (130, 136, 8)])
 def test_small_random(orc, dtype, M, N, K):
     check(orc, dtype, M, N, K, 1, 0, seed=1000 + M + N + K)
