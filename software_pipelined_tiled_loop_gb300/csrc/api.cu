@@ -219,6 +219,7 @@ __global__ void repack_rows_kernel(const uint8_t *__restrict__ src, long long sl
         for (long long b = nchunks * 16 + 2 * threadIdx.x; b < row_bytes; b += 2 * blockDim.x)
             *reinterpret_cast<uint16_t *>(d + b) = *reinterpret_cast<const uint16_t *>(s + b);
     }
+    grid_launch_dependents();  // this block's rows are written
 }
 
 static cudaError_t launch_repack(const void *src, long long sld, void *dst, long long dld,
@@ -356,6 +357,7 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
         if (encode_2d(&tc_map, ct, 4, C, N, M, N, 32, 32, true) == PGEMM_OK) tmap_c = &tc_map;
     }
 
+    const bool after_prepass = static_cast<bool>(prepass);
     cudaError_t e = prepass ? prepass() : cudaSuccess;
     if (e != cudaSuccess) return PGEMM_ERR_CUDA;
     KernelCtx ctx{d->status, kDefaultWaitLimitNs};
@@ -364,6 +366,7 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
         p.M = M; p.N = N; p.K = K; p.ldc = N; p.group_m = 0;
         p.sm_count = d->sm_count; p.blocks_per_sm = blocks_per_sm;
         p.tmap_a = &ta; p.tmap_b = &tb; p.tmap_c = tmap_c; p.ctx = ctx;
+        p.after_prepass = after_prepass;
         p.alpha = alpha; p.beta = beta; p.C = C;
         e = k->launch_f32(p, stream);
     } else if constexpr (KIND == Kind::BF16) {
@@ -371,6 +374,7 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
         p.M = M; p.N = N; p.K = K; p.ldc = N; p.group_m = 0;
         p.sm_count = d->sm_count; p.blocks_per_sm = blocks_per_sm;
         p.tmap_a = &ta; p.tmap_b = &tb; p.tmap_c = tmap_c; p.ctx = ctx;
+        p.after_prepass = after_prepass;
         p.alpha = alpha; p.beta = beta; p.C = C;
         e = k->launch_bf16(p, stream);
     } else {
@@ -378,6 +382,7 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
         p.M = M; p.N = N; p.K = K; p.ldc = N; p.group_m = 0;
         p.sm_count = d->sm_count; p.blocks_per_sm = blocks_per_sm;
         p.tmap_a = &ta; p.tmap_b = &tb; p.tmap_c = tmap_c; p.ctx = ctx;
+        p.after_prepass = after_prepass;
         p.alpha = alpha; p.beta = beta; p.C = C;
         e = k->launch_i8(p, stream);
     }

@@ -67,35 +67,25 @@ struct WidenJob {
 };
 
 // dst[r][c] = (fp16) src[r][c] for r < rows, c < cols, for the two operands
-// (blockIdx.y selects A or B).  32 values per thread per step on the vector
-// path, one value per thread otherwise.
+// (blockIdx.y selects A or B).  Vector path: each thread converts groups of 8
+// values (an 8-byte load, a 16-byte store), consecutive threads taking
+// consecutive groups, so every warp load and store is one contiguous run.
 __global__ void __launch_bounds__(256) widen_i8_to_f16_kernel(WidenJob ja, WidenJob jb) {
     const WidenJob &j = blockIdx.y == 0 ? ja : jb;
     if (j.rows <= 0 || j.cols <= 0) return;
     const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
     const long long t0 = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
     if (j.vec) {
-        const long long per_row = j.cols / 32 + ((j.cols % 32) ? 1 : 0);  // 32-wide pieces
-        const long long total = per_row * j.rows;
+        const int per_row = j.cols / 8;  // cols % 16 == 0 on this path
+        const long long total = static_cast<long long>(per_row) * j.rows;
         for (long long i = t0; i < total; i += stride) {
             const long long r = i / per_row;
-            const int c0 = static_cast<int>(i - r * per_row) * 32;
-            const int8_t *s = j.src + r * j.sld + c0;
-            __half *d = j.dst + r * j.dld + c0;
-            const int nvec = min(2, (j.cols - c0) / 16);  // 16-value vectors in this piece
-#pragma unroll
-            for (int v = 0; v < 2; ++v) {
-                if (v < nvec) {
-                    const uint4 w = reinterpret_cast<const uint4 *>(s)[v];
-                    __half2 o[8];
-                    widen4(w.x, o[0], o[1]);
-                    widen4(w.y, o[2], o[3]);
-                    widen4(w.z, o[4], o[5]);
-                    widen4(w.w, o[6], o[7]);
-                    reinterpret_cast<uint4 *>(d)[2 * v] = *reinterpret_cast<const uint4 *>(&o[0]);
-                    reinterpret_cast<uint4 *>(d)[2 * v + 1] = *reinterpret_cast<const uint4 *>(&o[4]);
-                }
-            }
+            const int c0 = static_cast<int>(i - r * per_row) * 8;
+            const uint2 w = *reinterpret_cast<const uint2 *>(j.src + r * j.sld + c0);
+            __half2 o[4];
+            widen4(w.x, o[0], o[1]);
+            widen4(w.y, o[2], o[3]);
+            *reinterpret_cast<uint4 *>(j.dst + r * j.dld + c0) = *reinterpret_cast<const uint4 *>(o);
         }
     } else {
         const long long total = static_cast<long long>(j.rows) * j.cols;
@@ -104,6 +94,7 @@ __global__ void __launch_bounds__(256) widen_i8_to_f16_kernel(WidenJob ja, Widen
             j.dst[r * j.dld + c] = __short2half_rn(static_cast<short>(j.src[r * j.sld + c]));
         }
     }
+    grid_launch_dependents();  // this block's share is written
 }
 
 static WidenJob make_job(const int8_t *src, long long sld, void *dst, long long dld, int rows,
@@ -123,11 +114,11 @@ cudaError_t launch_widen_i8_pair(const int8_t *a, long long lda, void *a_dst, lo
     const WidenJob ja = make_job(a, lda, a_dst, a_dld, a_rows, a_cols);
     const WidenJob jb = make_job(b, ldb, b_dst, b_dld, b_rows, b_cols);
     auto work = [](const WidenJob &j) -> long long {
-        return j.vec ? (static_cast<long long>(j.cols) / 32 + 1) * j.rows
+        return j.vec ? static_cast<long long>(j.cols / 8) * j.rows
                      : static_cast<long long>(j.rows) * j.cols;
     };
     long long items = work(ja) > work(jb) ? work(ja) : work(jb);
-    long long blocks = (items + 255) / 256;
+    long long blocks = (items + 1023) / 1024;  // about four groups per thread
     const long long cap = static_cast<long long>(sm_count) * 16;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;

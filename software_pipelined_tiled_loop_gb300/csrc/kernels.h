@@ -31,6 +31,7 @@ struct LaunchCommon {
     const CUtensorMap *tmap_a;
     const CUtensorMap *tmap_b;
     const CUtensorMap *tmap_c;  // C as a 32 x 32-box, 128-byte-swizzled map, or nullptr
+    bool after_prepass;         // a widening / repack kernel of this call precedes the GEMM
     KernelCtx ctx;
 };
 

@@ -374,6 +374,20 @@ __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// ------------------------------------------------ programmatic dependent launch ---
+// Wait until the grids this grid depends on (the previous kernel in the stream,
+// when launched with programmatic stream serialisation) have completed and
+// their memory is visible.  A no-op for an ordinary launch.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Let the dependent grid start launching (its blocks still wait in
+// grid_dependency_wait until this grid has completed).
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------ misc utils ---
 __device__ __forceinline__ bool elect_lane0() { return (threadIdx.x & 31u) == 0u; }
 

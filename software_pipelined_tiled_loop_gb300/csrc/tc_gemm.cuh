@@ -230,6 +230,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Everything above touched only on-chip state; global memory may still be
+    // being written by a pre-pass launched just before (widening, repack).
+    grid_dependency_wait();
 
     // Cluster geometry: with a CTA pair a "tile" of the schedule is a 2 x 1
     // stack of 128-row tiles; this CTA computes the one at its cluster rank.
@@ -491,29 +494,39 @@ static cudaError_t launch_tc(const P &p, cudaStream_t stream) {
     a.ldc = p.ldc;
     a.c_tma = p.tmap_c != nullptr ? 1 : 0;
     const CUtensorMap &tc = p.tmap_c != nullptr ? *p.tmap_c : *p.tmap_a;
+    // After a pre-pass of this call, launch with programmatic stream
+    // serialisation: the prologue overlaps the pre-pass's tail, and every
+    // thread waits for it (grid_dependency_wait) before touching memory.
+    cudaLaunchAttribute attr[2];
+    int nattr = 0;
+    if (p.after_prepass) {
+        attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[nattr].val.programmaticStreamSerializationAllowed = 1;
+        ++nattr;
+    }
+    cudaLaunchConfig_t lc{};
+    lc.blockDim = dim3(Cfg::THREADS);
+    lc.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    lc.stream = stream;
+    lc.attrs = attr;
     if constexpr (Cfg::CM == 1) {
         const int tiles = a.num_m_tiles * a.num_n_tiles;
         const int per_sm = p.blocks_per_sm < Cfg::MAX_BLOCKS ? p.blocks_per_sm : Cfg::MAX_BLOCKS;
         int grid = p.sm_count * (per_sm > 0 ? per_sm : 1);
         if (grid > tiles) grid = tiles;
         if (grid < 1) return cudaSuccess;
-        tc_gemm_kernel<Cfg><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(*p.tmap_a, *p.tmap_b,
-                                                                             tc, a, p.ctx);
-        return cudaGetLastError();
+        lc.gridDim = dim3(grid);
+        lc.numAttrs = nattr;
+        return cudaLaunchKernelEx(&lc, tc_gemm_kernel<Cfg>, *p.tmap_a, *p.tmap_b, tc, a, p.ctx);
     } else {
         // clusters of CM CTAs; as many as can be resident at once (persistent)
         const int sched_tiles = ((a.num_m_tiles + Cfg::CM - 1) / Cfg::CM) * a.num_n_tiles;
-        cudaLaunchConfig_t lc{};
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = Cfg::CM;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        lc.blockDim = dim3(Cfg::THREADS);
-        lc.dynamicSmemBytes = Cfg::SMEM_BYTES;
-        lc.stream = stream;
-        lc.attrs = attr;
-        lc.numAttrs = 1;
+        attr[nattr].id = cudaLaunchAttributeClusterDimension;
+        attr[nattr].val.clusterDim.x = Cfg::CM;
+        attr[nattr].val.clusterDim.y = 1;
+        attr[nattr].val.clusterDim.z = 1;
+        ++nattr;
+        lc.numAttrs = nattr;
         int clusters = 0;
         lc.gridDim = dim3(Cfg::CM * p.sm_count);
         cudaError_t e = cudaOccupancyMaxActiveClusters(&clusters, tc_gemm_kernel<Cfg>, &lc);
