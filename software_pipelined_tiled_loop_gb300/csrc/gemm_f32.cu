@@ -171,15 +171,22 @@ __global__ void __launch_bounds__(128, F32Cfg<BN_, STAGES>::MIN_BLOCKS)
                 const uint32_t brow = b_base + (k4 * 4 + kk) * (BN * 4);
 #pragma unroll
                 for (int g = 0; g < G; ++g) b[g] = lds128(brow + g * 64);
+                // the eight rows' A values, each broadcast to a pair
+                float2 a2[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const float av = kk == 0 ? a[i].x : kk == 1 ? a[i].y : kk == 2 ? a[i].z : a[i].w;
-                    const float2 a2 = make_float2(av, av);
+                    a2[i] = make_float2(av, av);
+                }
+                // B-pair-major order: consecutive FFMA2s share an operand pair
+                // (measured 62.4 vs 60.0 TFLOP/s for the row-major order)
 #pragma unroll
-                    for (int g = 0; g < G; ++g) {
-                        acc[i][2 * g] = __ffma2_rn(a2, make_float2(b[g].x, b[g].y), acc[i][2 * g]);
-                        acc[i][2 * g + 1] =
-                            __ffma2_rn(a2, make_float2(b[g].z, b[g].w), acc[i][2 * g + 1]);
+                for (int g = 0; g < G; ++g) {
+                    const float2 b0 = make_float2(b[g].x, b[g].y), b1 = make_float2(b[g].z, b[g].w);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        acc[i][2 * g] = __ffma2_rn(a2[i], b0, acc[i][2 * g]);
+                        acc[i][2 * g + 1] = __ffma2_rn(a2[i], b1, acc[i][2 * g + 1]);
                     }
                 }
             }
