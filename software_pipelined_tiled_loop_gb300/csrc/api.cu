@@ -126,9 +126,10 @@ static const KernelInfo *table_of(pgemm_dtype dt, int *count) {
 //  * bf16 and int8: 256 x 256 tiles on a CTA pair (cta_group::2) with six
 //    stages when the pairs cover the GPU (bf16 8192^3 +12 %, int8 4096^3
 //    +10 % over 128 x 256); else 128 x 256 with four stages when those tiles
-//    cover every SM; else 128 x 128.
+//    cover every SM; else 128 x 128.  At most two K-tiles (K <= 128): the call
+//    is bound by writing C, and 128 x 128 tiles with four stages (room for two
+//    epilogue staging buffers per warp) write it fastest.
 static pgemm_config default_config(pgemm_dtype dt, int M, int N, int K, int sm_count) {
-    (void)K;
     pgemm_config c{128, 128, 0, 4};
     if (dt == PGEMM_F32) {
         const long long tiles128 = (long long)((M + 127) / 128) * ((N + 127) / 128);
@@ -138,6 +139,7 @@ static pgemm_config default_config(pgemm_dtype dt, int M, int N, int K, int sm_c
     }
     const long long tiles256 = (long long)((M + 127) / 128) * ((N + 255) / 256);
     const long long pairs = (long long)((M + 255) / 256) * ((N + 255) / 256);
+    if (K <= 128) return c;  // 128 x 128, four stages
     if (pairs >= sm_count / 2) {
         c.bm = 256;
         c.bn = 256;

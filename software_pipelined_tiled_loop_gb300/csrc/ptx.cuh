@@ -145,10 +145,11 @@ __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 
-// Wait until every committed bulk store of this thread has finished reading
-// its shared-memory source.
-__device__ __forceinline__ void bulk_wait_read_all() {
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+// Wait until at most N committed bulk stores of this thread are still reading
+// their shared-memory sources (N = 0: all have finished reading).
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 
 // Wait until every committed bulk store of this thread has completed.

@@ -77,7 +77,11 @@ struct TcCfg {
     static constexpr int B_BYTES = B_COLS * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // per CTA
     static constexpr int TX_BYTES = STAGE_BYTES * CG;      // counted on the MMA's full barrier
-    static constexpr int STAGING_BYTES = EPI * 32 * 32 * 4;  // one 32x32 block per warp
+    // Epilogue staging: one or two 32x32 fp32 blocks per epilogue warp (two
+    // let a TMA store drain while the next block is staged), as many as fit.
+    static constexpr int STAGE_BUFS =
+        STAGES * STAGE_BYTES + EPI * 2 * 4096 + (2 * STAGES + 5) * 8 + 16 + 1024 <= 232448 ? 2 : 1;
+    static constexpr int STAGING_BYTES = EPI * STAGE_BUFS * 32 * 32 * 4;
     static constexpr int ACC_COLS = BN;        // fp32 accumulator: one TMEM column per n
     static constexpr int TMEM_COLS = 2 * BN;   // two accumulators
     static constexpr int THREADS = 64 + 32 * EPI;
@@ -109,7 +113,9 @@ struct TcCfg {
 //     beta == 0; the store clips rows/columns outside C), or
 //   - written by 32 coalesced row stores (lane l writes column col + l),
 //     predicated at the edges, reading C first when beta != 0.
-template <typename Scalar>
+// `buf` is this warp's staging buffer for this block: with NBUF = 2 buffers
+// used in turn, the store issued into the other buffer may still be reading.
+template <int NBUF, typename Scalar>
 __device__ __forceinline__ void store_block32(const GemmArgs<Scalar, Scalar> &a,
                                               const CUtensorMap *tmap_c, uint8_t *buf,
                                               int m_base, int col, const uint32_t *vals,
@@ -117,8 +123,8 @@ __device__ __forceinline__ void store_block32(const GemmArgs<Scalar, Scalar> &a,
     const uint32_t lane = lane_id();
     const uint32_t sbuf = smem_u32(buf);
     if (tma_path) {
-        // the previous store of this warp must have finished reading the buffer
-        if (lane == 0) bulk_wait_read_all();
+        // the store that last used this buffer must have finished reading it
+        if (lane == 0) bulk_wait_read<NBUF - 1>();
         __syncwarp();
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -360,7 +366,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         const uint32_t e = warp - 2;            // epilogue warp index
         const uint32_t q = warp & 3u;           // the TMEM lane quadrant this warp may read
         const int col0 = static_cast<int>(e >> 2) * Cfg::EPI_COLS;  // its column range
-        uint8_t *buf = sStage + e * (32 * 32 * 4);
+        uint8_t *wbuf = sStage + e * (Cfg::STAGE_BUFS * 32 * 32 * 4);  // this warp's buffers
+        uint32_t nstore = 0;  // blocks this warp has stored (selects the buffer)
+        auto next_buf = [&]() -> uint8_t * {
+            return wbuf + (nstore++ % Cfg::STAGE_BUFS) * (32 * 32 * 4);
+        };
         const bool tma_path = args.c_tma && args.beta == Scalar(0);
         uint32_t gr = 0;
         bool ok = true;
@@ -418,7 +428,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 if (in_range) {
 #pragma unroll
                     for (int c = 0; c < Cfg::EPI_COLS; c += 32)
-                        store_block32(args, &tmap_c, buf, m_base, n0 + col0 + c, acc + c,
+                        store_block32<Cfg::STAGE_BUFS>(args, &tmap_c, next_buf(), m_base, n0 + col0 + c, acc + c,
                                       rounds > 0, tma_path);
                 }
             } else {
@@ -440,7 +450,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                             if (lane == 0) release_acc<Cfg>(&acc_empty[ab]);
                         }
                         if (in_range)
-                            store_block32(args, &tmap_c, buf, m_base, n0 + col0 + c, v, true,
+                            store_block32<Cfg::STAGE_BUFS>(args, &tmap_c, next_buf(), m_base, n0 + col0 + c, v, true,
                                           tma_path);
                     }
                     ++gr;
@@ -451,7 +461,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     for (int j = 0; j < 32; ++j) zero[j] = 0u;
 #pragma unroll 1
                     for (int c = 0; in_range && c < Cfg::EPI_COLS; c += 32)
-                        store_block32(args, &tmap_c, buf, m_base, n0 + col0 + c, zero, false,
+                        store_block32<Cfg::STAGE_BUFS>(args, &tmap_c, next_buf(), m_base, n0 + col0 + c, zero, false,
                                       tma_path);
                 }
             }
