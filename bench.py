@@ -344,13 +344,15 @@ def run_point(dtype, M, N, K, recipe, cfg, steps, warmup, seed=None):
     ms = [a.elapsed_time(b) for a, b in ev]
     status = pg.pgemm_get_device_status()
     attrs = pg.pgemm_kernel_attrs(dtype, cfg)
+    sched = pg.pgemm_schedule(dtype, M, N, K, cfg)
     med = statistics.median(ms)
     flops = 2.0 * M * N * K
     out_bytes = M * N * 4 * (2 if beta != 0 else 1)
     in_bytes = (M * K + K * N) * {"f32": 4, "bf16": 2, "i8": 1}[dtype]
     del dA, dB, dC, flush
     return {"dtype": dtype, "M": M, "N": N, "K": K, "bm": cfg[0], "bn": cfg[1], "bk": cfg[2],
-            "stages": cfg[3], "k_tiles": -(-K // cfg[2]), **attrs, "ms_median": round(med, 4),
+            "stages": cfg[3], "max_k_parts": cfg[4] if len(cfg) > 4 else 0,
+            "k_tiles": -(-K // cfg[2]), **attrs, **sched, "ms_median": round(med, 4),
             "ms_min": round(min(ms), 4), "tflops": round(flops / (med * 1e-3) / 1e12, 2),
             "gbs": round((in_bytes + out_bytes) / (med * 1e-3) / 1e9, 1), "status": status}
 
@@ -502,7 +504,8 @@ def main():
     ap.add_argument("--hazard", type=int, default=0,
                     help="run the stage-reuse hazard experiment this many iterations per variant")
     ap.add_argument("--point", default=None,
-                    help="dtype,M,N,K,bm,bn,bk,stages: time one point (for profiler captures)")
+                    help="dtype,M,N,K,bm,bn,bk,stages[,max_k_parts]: time one point "
+                         "(for profiler captures and split / no-split comparisons)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
@@ -519,9 +522,10 @@ def main():
             sweep(args.sweep.split(","), args.steps, args.warmup, ks)
         else:
             f = args.point.split(",")
-            dt, (M, N, K, bm, bn, bk, st) = f[0], map(int, f[1:])
+            dt, nums = f[0], [int(x) for x in f[1:]]
+            M, N, K = nums[:3]
             recipe = {"f32": "f32_uniform_beta", "bf16": "bf16_normal", "i8": "i8_uniform"}[dt]
-            print(json.dumps(run_point(dt, M, N, K, recipe, (bm, bn, bk, st), args.steps,
+            print(json.dumps(run_point(dt, M, N, K, recipe, tuple(nums[3:]), args.steps,
                                        args.warmup)))
         return
 

@@ -25,7 +25,9 @@
  *     stream): it enqueues work and returns; the caller synchronises.  The
  *     library may enqueue a small repack kernel and stream-ordered scratch
  *     (cudaMallocAsync / cudaFreeAsync) on the same stream when a leading
- *     dimension is not a multiple of 16 bytes.
+ *     dimension is not a multiple of 16 bytes, and (bf16, int8) stream-ordered
+ *     scratch plus a cudaMemsetAsync of its counters when the last wave of
+ *     output tiles is split along K (see pgemm_config.max_k_parts).
  *   - M, N, K >= 0.  M == 0 or N == 0: nothing is done.  K == 0: C <- beta*C
  *     (C is not read when beta == 0, so a NaN in C does not survive).
  *   - beta == 0: C is not read (BLAS convention).
@@ -75,9 +77,20 @@ typedef enum { PGEMM_F32 = 0, PGEMM_BF16 = 1, PGEMM_I8 = 2 } pgemm_dtype;
  * number of pipeline stages (shared-memory ring slots).  Stage count trades
  * latency coverage against shared memory and resident blocks ("Software
  * pipelines and asynchronous copies", section "Selecting the number of
- * stages").  Zero fields mean "library default for this shape". */
+ * stages").  Zero fields mean "library default for this shape".
+ *
+ * max_k_parts (bf16 and int8; the pages have no counterpart): the tensor-core
+ * kernels are persistent, one work unit per resident CTA (or CTA pair) at a
+ * time.  When the output tiles would leave the last wave at most half full,
+ * as many tiles as that wave would hold are cut along K into P parts each
+ * (P <= resident units / those tiles, P <= 8, every part at least 1024 of K)
+ * and run first, side by side; the last part of a tile to finish adds the
+ * others' partial sums (fp32, in part order, so the result does not depend
+ * on timing; int8: exact int32) before the alpha/beta update.  max_k_parts =
+ * 0: that choice; 1: never split; n > 1: at most n parts.  fp32 ignores it. */
 typedef struct {
     int bm, bn, bk, stages;
+    int max_k_parts;
 } pgemm_config;
 
 /* fp32: FFMA register-tiled consumers on the pipelined ring.  Semantics are
@@ -155,6 +168,28 @@ PGEMM_API int pgemm_list_configs(pgemm_dtype dtype, pgemm_config *out, int cap);
 PGEMM_API pgemm_status pgemm_kernel_attrs(pgemm_dtype dtype, const pgemm_config *cfg, int *smem_bytes,
                                 int *regs_per_thread, int *threads_per_block,
                                 int *blocks_per_sm);
+
+/* The schedule a call with these arguments would use on the current device
+ * (cfg NULL = default configuration): output tiles (a CTA pair's 256-row tile
+ * counts once), schedule slots (units that run at once), tiles split along K
+ * and their parts (0 and 1 when nothing is split).  No GPU work is enqueued.
+ * Any output pointer may be NULL. */
+PGEMM_API pgemm_status pgemm_schedule(pgemm_dtype dtype, const pgemm_config *cfg, int M, int N,
+                                      int K, long long *tiles, int *slots,
+                                      long long *split_tiles, int *parts);
+
+/* The K-split rule itself, a pure host computation (no device needed): for
+ * `tiles` output tiles on `slots` schedule slots, K of `k_tiles` K-tiles and
+ * accumulation rounds of `round_tiles` K-tiles (0: one round per tile), with
+ * the cap `max_parts` (as in pgemm_config).  Outputs: how many tiles are
+ * split (0 when none; they are the first tiles of the schedule and run
+ * first), the parts per split tile (1 when none), the granule in K-tiles that
+ * parts are made of, and the number of whole granules in K.  Part j of a
+ * split tile covers granules [j * granules / parts, (j + 1) * granules /
+ * parts); the last part also the K-tiles beyond `granules` whole granules. */
+PGEMM_API pgemm_status pgemm_split_plan(long long tiles, int slots, int k_tiles, int round_tiles,
+                                        int max_parts, long long *split_tiles, int *parts,
+                                        int *gran, int *granules);
 
 /* The stage-reuse hazard experiment of "Software pipelines and asynchronous
  * copies" (section "Practice"): a two-stage copy-and-reduce over the rows of

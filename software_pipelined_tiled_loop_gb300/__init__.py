@@ -20,7 +20,7 @@ __all__ = [
     "gemm_bf16_ex", "gemm_i8_ex", "pgemm_default_config", "pgemm_list_configs",
     "pgemm_kernel_attrs", "pgemm_get_device_status", "pgemm_selftest_wait_timeout",
     "pgemm_status_string", "pgemm_version", "gemm_i8_noalloc", "NOALLOC_SCRATCH_BYTES",
-    "pgemm_stage_reuse_demo",
+    "pgemm_stage_reuse_demo", "pgemm_schedule", "pgemm_split_plan",
     "DTYPES", "STATUS", "EXPORTED",
 ]
 
@@ -40,7 +40,8 @@ EXPORTED = [
     "gemm_f32", "gemm_bf16", "gemm_i8", "gemm_f32_ex", "gemm_bf16_ex", "gemm_i8_ex",
     "pgemm_default_config", "pgemm_list_configs", "pgemm_kernel_attrs",
     "pgemm_get_device_status", "pgemm_selftest_wait_timeout", "pgemm_status_string",
-    "pgemm_version", "gemm_i8_noalloc", "pgemm_stage_reuse_demo",
+    "pgemm_version", "gemm_i8_noalloc", "pgemm_stage_reuse_demo", "pgemm_schedule",
+    "pgemm_split_plan",
 ]
 
 
@@ -53,10 +54,12 @@ class PgemmError(RuntimeError):
 
 
 class Config(ctypes.Structure):
+    """pgemm_config.  A tuple (bm, bn, bk, stages[, max_k_parts]) converts to it."""
     _fields_ = [("bm", ctypes.c_int), ("bn", ctypes.c_int), ("bk", ctypes.c_int),
-                ("stages", ctypes.c_int)]
+                ("stages", ctypes.c_int), ("max_k_parts", ctypes.c_int)]
 
     def as_tuple(self):
+        """(bm, bn, bk, stages): the kernel the configuration names."""
         return (self.bm, self.bn, self.bk, self.stages)
 
 
@@ -66,8 +69,10 @@ _lib = None
 
 def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
     i, f, vp, i32 = ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_int32
+    ll = ctypes.c_longlong
     cfgp = ctypes.POINTER(Config)
     ip = ctypes.POINTER(ctypes.c_int)
+    llp = ctypes.POINTER(ctypes.c_longlong)
     sig = {
         "gemm_f32": [i, i, i, f, vp, vp, f, vp, vp],
         "gemm_bf16": [i, i, i, f, vp, vp, f, vp, vp],
@@ -84,6 +89,8 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
         "pgemm_status_string": [i],
         "pgemm_version": [],
         "pgemm_stage_reuse_demo": [vp, i, i, vp, vp, i, i, ctypes.c_uint, vp, i, vp],
+        "pgemm_schedule": [i, cfgp, i, i, i, llp, ip, llp, ip],
+        "pgemm_split_plan": [ll, i, i, i, i, llp, ip, ip, ip],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -144,8 +151,7 @@ def _cfg(config):
         return None
     if isinstance(config, Config):
         return ctypes.byref(config)
-    bm, bn, bk, stages = config
-    return ctypes.byref(Config(bm, bn, bk, stages))
+    return ctypes.byref(Config(*config))
 
 
 def gemm_f32(M, N, K, alpha, A, B, beta, C, stream=None):
@@ -201,6 +207,27 @@ def pgemm_stage_reuse_demo(X, rows, cols, perm, out, check_reuse, delay_warp=-1,
                                         int(check_reuse), int(delay_warp), int(delay_ns),
                                         _ptr(trace), int(trace_cap), _stream(stream)),
            "pgemm_stage_reuse_demo")
+
+
+def pgemm_schedule(dtype: str, M: int, N: int, K: int, config=None):
+    """The persistent schedule of a call on the current device: a dict with
+    tiles, slots (units running at once), split_tiles and parts."""
+    t, sl, st, p = ctypes.c_longlong(), ctypes.c_int(), ctypes.c_longlong(), ctypes.c_int()
+    _check(lib().pgemm_schedule(DTYPES[dtype], _cfg(config), M, N, K, ctypes.byref(t),
+                                ctypes.byref(sl), ctypes.byref(st), ctypes.byref(p)),
+           "pgemm_schedule")
+    return {"tiles": t.value, "slots": sl.value, "split_tiles": st.value, "parts": p.value}
+
+
+def pgemm_split_plan(tiles: int, slots: int, k_tiles: int, round_tiles: int = 0,
+                     max_parts: int = 0):
+    """The K-split rule (host only): a dict with split_tiles, parts, gran and
+    granules."""
+    sf, p, g, q = ctypes.c_longlong(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(lib().pgemm_split_plan(tiles, slots, k_tiles, round_tiles, max_parts,
+                                  ctypes.byref(sf), ctypes.byref(p), ctypes.byref(g),
+                                  ctypes.byref(q)), "pgemm_split_plan")
+    return {"split_tiles": sf.value, "parts": p.value, "gran": g.value, "granules": q.value}
 
 
 def pgemm_default_config(dtype: str, M: int, N: int, K: int):

@@ -150,6 +150,38 @@ static pgemm_config default_config(pgemm_dtype dt, int M, int N, int K, int sm_c
     return c;
 }
 
+// Splitting tiles along K against wave quantisation.  A persistent grid of G
+// slots runs `tiles` output tiles in ceil(tiles / G) waves; when the last
+// wave would hold R = tiles % G tiles, at most G / 2, R tiles are instead cut
+// into P = min(G / R, granules of K, 8) parts each, so that the extra wave
+// takes about 1/P of a tile's time instead of a whole one.  The parts run
+// first (the R * P parts fill the first wave, the whole tiles follow), so
+// the exchange of partial sums overlaps whole-tile work in the slots instead
+// of ending the kernel.  A part is at least kSplitGranTiles K-tiles (or one
+// int8 round): below that the exchange costs about what it saves.
+constexpr int kSplitGranTiles = 16;
+constexpr int kMaxSplitParts = 8;
+
+static TileSchedule plan_schedule(const KernelInfo &k, int M, int N, int K, int slots,
+                                  int max_parts) {
+    TileSchedule s;
+    s.tiles = static_cast<long long>((M + k.bm - 1) / k.bm) * ((N + k.bn - 1) / k.bn);
+    s.slots = slots;
+    s.units = s.tiles;
+    if (k.schedule_slots == nullptr) return s;
+    const int T = (K + k.bk - 1) / k.bk;
+    if (pgemm_split_plan(s.tiles, slots, T, k.kc, max_parts, &s.split_tiles, &s.parts, &s.gran,
+                         &s.q) != PGEMM_OK)
+        return s;
+    const long long rem = s.split_tiles;
+    s.units = s.tiles + rem * (s.parts - 1);
+    if (s.parts > 1) {
+        s.partial_words = rem * s.parts * k.bm * k.bn;
+        s.counter_words = rem * k.slabs_per_tile * 2;
+    }
+    return s;
+}
+
 static const KernelInfo *find_kernel(pgemm_dtype dt, const pgemm_config &c) {
     int n = 0;
     const KernelInfo *t = table_of(dt, &n);
@@ -268,11 +300,25 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
 
     pgemm_config c = (cfg_in && cfg_in->stages > 0) ? *cfg_in : default_config(DT, M, N, K, d->sm_count);
     if (c.bm == 0) c.bm = 128;
+    if (cfg_in) c.max_k_parts = cfg_in->max_k_parts;
+    if (c.max_k_parts < 0) return PGEMM_ERR_INVALID_VALUE;
     const KernelInfo *k = find_kernel(DT, c);
     if (!k) return PGEMM_ERR_UNSUPPORTED_CONFIG;
     int blocks_per_sm = 0;
     st = kernel_setup(*d, *k, &blocks_per_sm);
     if (st != PGEMM_OK) return st;
+
+    // The persistent schedule (tensor-core kernels).  A call with a fixed
+    // scratch buffer does not split: the exchange area would need memory.
+    TileSchedule sched;
+    if (k->schedule_slots != nullptr) {
+        LaunchCommon q{};
+        q.sm_count = d->sm_count;
+        q.blocks_per_sm = blocks_per_sm;
+        int slots = 0;
+        if (k->schedule_slots(q, &slots) != cudaSuccess) return PGEMM_ERR_CUDA;
+        sched = plan_schedule(*k, M, N, K, slots, fixed_scratch != nullptr ? 1 : c.max_k_parts);
+    }
 
     // Operands as the kernels read them: element type, pitch, base pointer.
     const int in_bytes = KIND == Kind::F32 ? 4 : 2;  // int8 is widened to fp16
@@ -282,6 +328,19 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
     long long a_ld = lda, b_ld = ldb;
     Scratch scratch;
     scratch.s = stream;
+    Scratch split_area;  // partial sums and counters of K-split tiles
+    split_area.s = stream;
+    if (sched.parts > 1) {
+        const long long pbytes = round_up(sched.partial_words * 4, 256);
+        const long long cbytes = round_up(sched.counter_words * 4, 256);
+        if (cudaMallocAsync(&split_area.p, pbytes + cbytes, stream) != cudaSuccess)
+            return PGEMM_ERR_CUDA;
+        sched.partials = static_cast<uint32_t *>(split_area.p);
+        sched.counters = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(split_area.p) + pbytes);
+        // before any pre-pass, so that a programmatic launch after the pre-pass
+        // still finds the counters zero
+        if (cudaMemsetAsync(sched.counters, 0, cbytes, stream) != cudaSuccess) return PGEMM_ERR_CUDA;
+    }
     std::function<cudaError_t()> prepass;  // repack / widening launch, if any
     if (K > 0) {
         const long long align_elems = 16 / in_bytes;
@@ -377,6 +436,7 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
         p.sm_count = d->sm_count; p.blocks_per_sm = blocks_per_sm;
         p.tmap_a = &ta; p.tmap_b = &tb; p.tmap_c = tmap_c; p.ctx = ctx;
         p.after_prepass = after_prepass;
+        p.sched = sched;
         p.alpha = alpha; p.beta = beta; p.C = C;
         e = k->launch_bf16(p, stream);
     } else {
@@ -385,6 +445,7 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
         p.sm_count = d->sm_count; p.blocks_per_sm = blocks_per_sm;
         p.tmap_a = &ta; p.tmap_b = &tb; p.tmap_c = tmap_c; p.ctx = ctx;
         p.after_prepass = after_prepass;
+        p.sched = sched;
         p.alpha = alpha; p.beta = beta; p.C = C;
         e = k->launch_i8(p, stream);
     }
@@ -464,7 +525,7 @@ pgemm_status pgemm_default_config(pgemm_dtype dtype, int M, int N, int K, pgemm_
 int pgemm_list_configs(pgemm_dtype dtype, pgemm_config *out, int cap) {
     int n = 0;
     const KernelInfo *t = table_of(dtype, &n);
-    for (int i = 0; i < n && i < cap && out; ++i) out[i] = pgemm_config{t[i].bm, t[i].bn, t[i].bk, t[i].stages};
+    for (int i = 0; i < n && i < cap && out; ++i) out[i] = pgemm_config{t[i].bm, t[i].bn, t[i].bk, t[i].stages, 0};
     return n;
 }
 
@@ -489,6 +550,66 @@ pgemm_status pgemm_kernel_attrs(pgemm_dtype dtype, const pgemm_config *cfg, int 
     if (regs_per_thread) *regs_per_thread = fa.numRegs;
     if (threads_per_block) *threads_per_block = k->threads;
     if (blocks_per_sm) *blocks_per_sm = bps;
+    return PGEMM_OK;
+}
+
+pgemm_status pgemm_split_plan(long long tiles, int slots, int k_tiles, int round_tiles,
+                              int max_parts, long long *split_tiles, int *parts, int *gran,
+                              int *granules) {
+    if (tiles < 0 || slots < 1 || k_tiles < 0 || round_tiles < 0 || max_parts < 0 ||
+        !split_tiles || !parts || !gran || !granules)
+        return PGEMM_ERR_INVALID_VALUE;
+    *split_tiles = 0;
+    *parts = 1;
+    *gran = round_tiles > 0 ? round_tiles : kSplitGranTiles;
+    *granules = k_tiles / *gran;
+    if (max_parts == 1 || slots < 2 || *granules < 2) return PGEMM_OK;
+    const long long rem = tiles % slots;
+    if (rem == 0) return PGEMM_OK;
+    long long p = slots / rem;
+    if (p > *granules) p = *granules;
+    if (p > kMaxSplitParts) p = kMaxSplitParts;
+    if (max_parts > 1 && p > max_parts) p = max_parts;
+    if (p < 2) return PGEMM_OK;
+    *parts = static_cast<int>(p);
+    *split_tiles = rem;
+    return PGEMM_OK;
+}
+
+pgemm_status pgemm_schedule(pgemm_dtype dtype, const pgemm_config *cfg, int M, int N, int K,
+                            long long *tiles, int *slots, long long *split_tiles, int *parts) {
+    if (M < 0 || N < 0 || K < 0) return PGEMM_ERR_INVALID_VALUE;
+    if (dtype != PGEMM_F32 && dtype != PGEMM_BF16 && dtype != PGEMM_I8) return PGEMM_ERR_INVALID_VALUE;
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    DeviceState *d = nullptr;
+    pgemm_status st = device_setup(&dev, &d);
+    if (st != PGEMM_OK) return st;
+    pgemm_config c = (cfg && cfg->stages > 0) ? *cfg : default_config(dtype, M, N, K, d->sm_count);
+    if (c.bm == 0) c.bm = 128;
+    if (cfg) c.max_k_parts = cfg->max_k_parts;
+    if (c.max_k_parts < 0) return PGEMM_ERR_INVALID_VALUE;
+    const KernelInfo *k = find_kernel(dtype, c);
+    if (!k) return PGEMM_ERR_UNSUPPORTED_CONFIG;
+    int bps = 0;
+    st = kernel_setup(*d, *k, &bps);
+    if (st != PGEMM_OK) return st;
+    TileSchedule s;
+    if (k->schedule_slots != nullptr) {
+        LaunchCommon q{};
+        q.sm_count = d->sm_count;
+        q.blocks_per_sm = bps;
+        int n = 0;
+        if (k->schedule_slots(q, &n) != cudaSuccess) return PGEMM_ERR_CUDA;
+        s = plan_schedule(*k, M, N, K, n, c.max_k_parts);
+    } else {
+        s.tiles = static_cast<long long>((M + k->bm - 1) / k->bm) * ((N + k->bn - 1) / k->bn);
+        s.slots = d->sm_count * bps;
+    }
+    if (tiles) *tiles = s.tiles;
+    if (slots) *slots = s.slots;
+    if (split_tiles) *split_tiles = s.split_tiles;
+    if (parts) *parts = s.parts;
     return PGEMM_OK;
 }
 

@@ -19,6 +19,7 @@ enum WaitSite : uint32_t {
     kSiteConvertFull = 7,     // int8 widening warps waiting for a staged int8 tile
     kSiteConvertEmpty = 8,    // int8 widening warps waiting for a free fp16 slot
     kSiteSelfTest = 9,        // pgemm_selftest_wait_timeout
+    kSiteSplitPartial = 10,   // last part of a K-split tile waiting for the others' partials
 };
 
 // Problem description passed by value to every kernel.
@@ -31,6 +32,18 @@ struct GemmArgs {
     Out *C;           // row-major, leading dimension ldc
     long long ldc;
     int c_tma;        // 1: C is also described by a tensor map (TMA stores allowed)
+    // Work units of the persistent tensor-core kernels, strided over the grid.
+    // The first split_tiles output tiles are each cut along K into
+    // split_parts parts and come first: unit i * split_parts + j is part j of
+    // tile i and covers granules [j * split_q / split_parts, (j + 1) *
+    // split_q / split_parts) of split_gran K-tiles each, the last part also
+    // the K-tiles beyond split_q granules.  Then every other tile is one
+    // unit.  The parts of a tile meet through `partials` (raw partial sums)
+    // and `counters` (two per epilogue slab, zero at launch).  No split:
+    // split_tiles = 0, split_parts = 1.
+    int num_units, split_tiles, split_parts, split_gran, split_q;
+    uint32_t *partials;
+    uint32_t *counters;
 };
 
 // Output tile `tile` -> (m0, n0).  Tiles are visited in groups of `group_m`

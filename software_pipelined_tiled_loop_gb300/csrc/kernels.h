@@ -22,6 +22,25 @@ constexpr int smem_request(int used, int max_blocks) {
     return used > cap ? used : cap;
 }
 
+// How a call's output tiles are spread over a persistent tensor-core grid:
+// `slots` units run at once (resident CTAs, or CTA pairs); when the tiles
+// would leave the last wave at most half full, that many tiles
+// (`split_tiles`) are each cut along K into `parts` parts (whole granules of
+// `gran` K-tiles, `q` granules covering K) and scheduled first.
+// partials / counters: the split tiles' meeting area (counters zeroed before
+// the launch).
+struct TileSchedule {
+    long long tiles = 0;
+    int slots = 0;
+    long long split_tiles = 0;
+    int parts = 1;
+    int gran = 1, q = 0;
+    long long units = 0;
+    long long partial_words = 0, counter_words = 0;
+    uint32_t *partials = nullptr;
+    uint32_t *counters = nullptr;
+};
+
 struct LaunchCommon {
     int M, N, K;
     long long ldc;
@@ -33,6 +52,7 @@ struct LaunchCommon {
     const CUtensorMap *tmap_c;  // C as a 32 x 32-box, 128-byte-swizzled map, or nullptr
     bool after_prepass;         // a widening / repack kernel of this call precedes the GEMM
     KernelCtx ctx;
+    TileSchedule sched;         // tensor-core kernels only
 };
 
 struct LaunchBf16 : LaunchCommon {
@@ -58,6 +78,12 @@ struct KernelInfo {
     int a_box_x = 0, a_box_y = 0, b_box_x = 0, b_box_y = 0;
     bool a_swizzle128 = true, b_swizzle128 = true;
     bool c_tma = false;  // the kernel can store C through a tensor map
+    // Persistent tensor-core kernels: K-tiles per accumulation round (0 = all
+    // of K) and the number of schedule slots (resident CTAs or CTA pairs) for
+    // a launch; nullptr for the fp32 kernels, which do not split K.
+    int kc = 0;
+    int slabs_per_tile = 0;  // epilogue warps per tile (all CTAs of a pair)
+    cudaError_t (*schedule_slots)(const LaunchCommon &, int *slots) = nullptr;
     const void *func = nullptr;
     cudaError_t (*launch_bf16)(const LaunchBf16 &, cudaStream_t) = nullptr;
     cudaError_t (*launch_f32)(const LaunchF32 &, cudaStream_t) = nullptr;

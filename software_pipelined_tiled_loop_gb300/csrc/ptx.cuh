@@ -389,6 +389,36 @@ __device__ __forceinline__ void grid_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// ------------------------------------------- global-memory handoff (GPU scope) ---
+// Release increment: every memory operation this thread performed (and, via
+// a preceding warp or block barrier, those of the threads it synchronised
+// with) is visible to a thread that acquire-reads the new value.
+__device__ __forceinline__ void red_release_add(uint32_t *p, uint32_t v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Wait until *p >= target (acquire).  Bounded like mbar_wait: after
+// ctx.wait_limit_ns it records a timeout tagged with `site` and returns false.
+__device__ __forceinline__ bool wait_counter(const uint32_t *p, uint32_t target,
+                                             const KernelCtx &ctx, uint32_t site) {
+    if (ld_acquire(p) >= target) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (ld_acquire(p) < target) {
+        if (globaltimer_ns() - t0 > ctx.wait_limit_ns) {
+            atomicCAS(ctx.status, 0u, kStatusTimeout | (site & 0xffffu));
+            return false;
+        }
+        __nanosleep(64);
+    }
+    return true;
+}
+
 // ------------------------------------------------------------ misc utils ---
 __device__ __forceinline__ bool elect_lane0() { return (threadIdx.x & 31u) == 0u; }
 

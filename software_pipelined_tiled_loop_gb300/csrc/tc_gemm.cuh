@@ -28,11 +28,14 @@
 // products of int8 values stay integers of magnitude <= 2^24 and are exact;
 // the epilogue converts each chunk to int32 and adds it into registers).
 //
-// The kernel is persistent (grid = resident blocks, output tiles strided by
-// the grid) and TMEM holds two accumulators, so the epilogue of one round
-// overlaps the main loop of the next.  Stage index t % S and phase parity
-// (t / S) & 1 come from a running counter, valid for any S (the page's XOR
-// swap is valid for two stages only).
+// The kernel is persistent (grid = resident blocks, work units strided by
+// the grid; the pipeline prologue is paid once per block, not once per tile)
+// and TMEM holds two accumulators, so the epilogue of one round overlaps the
+// main loop of the next.  A work unit is an output tile, or one K part of a
+// tile split against wave quantisation (GemmArgs); the parts of a split tile
+// run first and meet through global memory (SplitSlab).  Stage index t % S
+// and phase parity (t / S) & 1 come from a running counter, valid for any S
+// (the page's XOR swap is valid for two stages only).
 //
 // Shared-memory layouts (both 128-byte swizzled, written by TMA):
 //   A stage: BM = 128 rows (m) x 64 elements (k) -> K-major operand: rows of
@@ -177,6 +180,152 @@ __device__ __forceinline__ void release_acc(uint64_t *acc_empty_bar) {
         mbar_arrive(acc_empty_bar);
 }
 
+// One work unit of the persistent schedule: an output tile (schedule index)
+// and the K-tiles [kb, ke) it accumulates; part >= 0 for a part of a tile
+// split along K (`split` numbers the split tiles from 0).
+struct WorkUnit {
+    int tile, kb, ke, part, split;
+};
+
+template <typename A>
+__device__ __forceinline__ WorkUnit work_unit(int u, const A &a) {
+    WorkUnit w;
+    const int split_units = a.split_tiles * a.split_parts;
+    if (u >= split_units) {
+        w.tile = u - split_units + a.split_tiles;
+        w.kb = 0;
+        w.ke = a.num_k_tiles;
+        w.part = -1;
+        w.split = 0;
+        return w;
+    }
+    w.split = u / a.split_parts;
+    w.part = u - w.split * a.split_parts;
+    w.tile = w.split;
+    w.kb = w.part * a.split_q / a.split_parts * a.split_gran;
+    w.ke = w.part == a.split_parts - 1 ? a.num_k_tiles
+                                       : (w.part + 1) * a.split_q / a.split_parts * a.split_gran;
+    return w;
+}
+
+// Accumulation rounds of a unit: chunks of KC K-tiles, or all of its K range.
+template <class Cfg>
+__device__ __forceinline__ int unit_round_tiles(const WorkUnit &w) {
+    return Cfg::KC > 0 ? Cfg::KC : (w.ke > w.kb ? w.ke - w.kb : 1);
+}
+template <class Cfg>
+__device__ __forceinline__ int unit_rounds(const WorkUnit &w) {
+    const int kct = unit_round_tiles<Cfg>(w);
+    return w.ke > w.kb ? (w.ke - w.kb + kct - 1) / kct : 0;
+}
+
+// Where the parts of a K-split tile meet, for one epilogue warp's slab of
+// 32 rows x EPI_COLS columns: one slot of raw partial sums per part and two
+// counters (parts arrived, partials written).  A warp arrives once its own
+// sums are in registers.  Every part but the last to arrive stores its
+// partial into its slot and then counts it written (release); the last one
+// waits until all the others are written (acquire) and adds them, in part
+// order, to its own before the alpha/beta update.  The parts it waits for
+// have arrived, so they are past every wait of their own: the exchange cannot
+// deadlock whatever part of the grid is resident, and nobody waits on a part
+// that has not started.
+//
+// Slot layout: 16-byte group g (columns 4g .. 4g+3) of row r at word
+// (g * 32 + r) * 4, so that each store or load of a warp covers 512
+// consecutive bytes.
+template <class Cfg>
+struct SplitSlab {
+    static constexpr int kSlotWords = 32 * Cfg::EPI_COLS;
+    uint32_t *slots;      // part 0's slot; part j's at slots + j * kSlotWords
+    uint32_t *counters;   // [0] parts arrived, [1] partials written
+    int parts, part;
+    bool last;
+
+    __device__ __forceinline__ SplitSlab() : slots(nullptr), counters(nullptr), parts(1), part(0), last(true) {}
+
+    template <typename A>
+    __device__ __forceinline__ SplitSlab(const A &a, const WorkUnit &w, uint32_t crank, uint32_t e) {
+        const long long slab = (static_cast<long long>(w.split) * Cfg::CM + crank) * Cfg::EPI + e;
+        parts = a.split_parts;
+        part = w.part;
+        slots = a.partials + slab * parts * kSlotWords;
+        counters = a.counters + 2 * slab;
+        uint32_t old = 0;
+        if (lane_id() == 0) old = atomicAdd(counters, 1u);
+        old = __shfl_sync(0xffffffffu, old, 0);
+        last = old == static_cast<uint32_t>(parts - 1);
+    }
+
+    // The last part: wait until every other part's partial is written.
+    __device__ __forceinline__ bool wait_others(const KernelCtx &ctx) const {
+        bool ok = true;
+        if (lane_id() == 0)
+            ok = wait_counter(counters + 1, static_cast<uint32_t>(parts - 1), ctx, kSiteSplitPartial);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        __syncwarp();
+        __threadfence();
+        return ok;
+    }
+
+    // Store 32 columns [c, c + 32) of this lane's row as this part's partial.
+    __device__ __forceinline__ void put(int c, const uint32_t *v) const {
+        uint4 *dst = reinterpret_cast<uint4 *>(slots + part * kSlotWords) + (c / 4) * 32 + lane_id();
+#pragma unroll
+        for (int g = 0; g < 8; ++g)
+            dst[g * 32] = make_uint4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+    }
+
+    // After the last put: count this partial as written.
+    __device__ __forceinline__ void publish() const {
+        __threadfence();
+        __syncwarp();
+        if (lane_id() == 0) red_release_add(counters + 1, 1u);
+    }
+
+    // Part j's 32 columns [c, c + 32) of this lane's row (j != part).
+    __device__ __forceinline__ void get(int j, int c, uint32_t *v) const {
+        const uint4 *src =
+            reinterpret_cast<const uint4 *>(slots + j * kSlotWords) + (c / 4) * 32 + lane_id();
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+            const uint4 x = __ldcg(src + g * 32);
+            v[4 * g] = x.x;
+            v[4 * g + 1] = x.y;
+            v[4 * g + 2] = x.z;
+            v[4 * g + 3] = x.w;
+        }
+    }
+
+    // v <- the sum over all parts of columns [c, c + 32), v holding this
+    // part's own values on entry.  fp32: added in part order, P0 + P1 + ...,
+    // whichever part arrived last, so the result does not depend on timing.
+    __device__ __forceinline__ void reduce_f32(int c, uint32_t *v) const {
+        float sum[32];
+        uint32_t t[32];
+        for (int j = 0; j < parts; ++j) {
+            if (j != part) get(j, c, t);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float x = __uint_as_float(j == part ? v[i] : t[i]);
+                sum[i] = j == 0 ? x : sum[i] + x;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(sum[i]);
+    }
+
+    // int32: v += every other part's values, modulo 2^32 (order-free).
+    __device__ __forceinline__ void reduce_i32(int c, uint32_t *v) const {
+        uint32_t t[32];
+        for (int j = 0; j < parts; ++j) {
+            if (j == part) continue;
+            get(j, c, t);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] += t[i];
+        }
+    }
+};
+
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
@@ -246,23 +395,20 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     const int sched_id = static_cast<int>(blockIdx.x) / Cfg::CM;
     const int sched_stride = static_cast<int>(gridDim.x) / Cfg::CM;
     const int num_m_sched = (args.num_m_tiles + Cfg::CM - 1) / Cfg::CM;
-    const int num_tiles = num_m_sched * args.num_n_tiles;
-    const int T = args.num_k_tiles;
-    // accumulation rounds per output tile
-    const int KCt = Cfg::KC > 0 ? Cfg::KC : (T > 0 ? T : 1);
-    const int rounds = T > 0 ? (T + KCt - 1) / KCt : 0;
+    const int num_units = args.num_units;
 
     if (warp == 0) {
         if (lane == 0) {
             // ---------------- producer: TMA into the stage ring ----------------
             uint32_t it = 0;
             bool ok = true;
-            for (int tile = sched_id; ok && tile < num_tiles; tile += sched_stride) {
+            for (int u = sched_id; ok && u < num_units; u += sched_stride) {
+                const WorkUnit w = work_unit(u, args);
                 int m0, n0;
-                tile_origin(tile, num_m_sched, args.num_n_tiles, args.group_m, BM * Cfg::CM, BN, m0,
+                tile_origin(w.tile, num_m_sched, args.num_n_tiles, args.group_m, BM * Cfg::CM, BN, m0,
                             n0);
                 m0 += static_cast<int>(crank) * BM;
-                for (int kt = 0; kt < T; ++kt, ++it) {
+                for (int kt = w.kb; kt < w.ke; ++kt, ++it) {
                     const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
                     if (!mbar_wait(&empty[s], ph ^ 1u, ctx, kSiteProducerEmpty)) {
                         ok = false;
@@ -310,7 +456,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             constexpr uint16_t kPair = 3;  // both CTAs of the pair
             uint32_t it = 0, gr = 0;
             bool ok = true;
-            for (int tile = sched_id; ok && tile < num_tiles; tile += sched_stride) {
+            for (int u = sched_id; ok && u < num_units; u += sched_stride) {
+                const WorkUnit w = work_unit(u, args);
+                const int kct = unit_round_tiles<Cfg>(w);
+                const int rounds = unit_rounds<Cfg>(w);
                 for (int r = 0; ok && r < rounds; ++r, ++gr) {
                     const uint32_t ab = gr & 1u, aph = (gr >> 1) & 1u;
                     if (!mbar_wait(&acc_empty[ab], aph ^ 1u, ctx, kSiteMmaAccEmpty)) {
@@ -319,8 +468,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + ab * Cfg::ACC_COLS;
-                    const int k_end = min(T, (r + 1) * KCt);
-                    for (int kt = r * KCt; kt < k_end; ++kt, ++it) {
+                    const int k_begin = w.kb + r * kct;
+                    const int k_end = min(w.ke, k_begin + kct);
+                    for (int kt = k_begin; kt < k_end; ++kt, ++it) {
                         const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
                         if (!mbar_wait(&full[s], ph, ctx, kSiteMmaFull)) {
                             ok = false;
@@ -329,7 +479,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         tc_fence_after();
                         const uint32_t a_addr = smem_u32(sA + s * Cfg::A_BYTES);
                         const uint32_t b_addr = smem_u32(sB + s * Cfg::B_BYTES);
-                        const bool first = kt == r * KCt;
+                        const bool first = kt == k_begin;
 #pragma unroll
                         for (int k = 0; k < BK / 16; ++k) {
                             const uint64_t ad = smem_desc_sw128(a_addr + k * 32, 16, 1024);
@@ -374,12 +524,17 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         const bool tma_path = args.c_tma && args.beta == Scalar(0);
         uint32_t gr = 0;
         bool ok = true;
-        for (int tile = sched_id; ok && tile < num_tiles; tile += sched_stride) {
+        for (int u = sched_id; ok && u < num_units; u += sched_stride) {
+            const WorkUnit w = work_unit(u, args);
+            const int rounds = unit_rounds<Cfg>(w);
             int m0, n0;
-            tile_origin(tile, num_m_sched, args.num_n_tiles, args.group_m, BM * Cfg::CM, BN, m0, n0);
+            tile_origin(w.tile, num_m_sched, args.num_n_tiles, args.group_m, BM * Cfg::CM, BN, m0, n0);
             m0 += static_cast<int>(crank) * BM;
             const bool in_range = m0 < args.M;  // the second tile of a pair may lie below C
             const int m_base = m0 + static_cast<int>(q * 32);
+            // A part of a K-split tile exchanges partial sums (rows below C,
+            // the same for every part, take no part in it).
+            const bool split = w.part >= 0 && in_range;
             if constexpr (Cfg::INT_FOLD) {
                 // Exact int8: sum the rounds' integer-valued fp32 partials in
                 // int32.  Rounds of at most 256 products (|x| <= 2^22) convert
@@ -425,6 +580,18 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     kMagicFold ? static_cast<uint32_t>(rounds) * 0x4B400000u : 0u;  // mod 2^32
 #pragma unroll
                 for (int j = 0; j < Cfg::EPI_COLS; ++j) acc[j] -= bias;
+                if (split) {
+                    const SplitSlab<Cfg> slab(args, w, crank, e);
+                    if (!slab.last) {
+#pragma unroll
+                        for (int c = 0; c < Cfg::EPI_COLS; c += 32) slab.put(c, acc + c);
+                        slab.publish();
+                        continue;
+                    }
+                    if (!slab.wait_others(ctx)) break;
+#pragma unroll
+                    for (int c = 0; c < Cfg::EPI_COLS; c += 32) slab.reduce_i32(c, acc + c);
+                }
                 if (in_range) {
 #pragma unroll
                     for (int c = 0; c < Cfg::EPI_COLS; c += 32)
@@ -438,6 +605,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     tc_fence_after();
                     const uint32_t t_row =
                         tmem_base + ((q * 32u) << 16) + ab * Cfg::ACC_COLS + col0;
+                    // role in a K-split tile: store a partial, or add them all
+                    int role = 0;  // 0: whole tile, 1: store partial, 2: reduce
+                    SplitSlab<Cfg> slab = split ? SplitSlab<Cfg>(args, w, crank, e) : SplitSlab<Cfg>();
+                    if (split) {
+                        role = slab.last ? 2 : 1;
+                        if (role == 2 && !slab.wait_others(ctx)) ok = false;
+                    }
 #pragma unroll 1
                     for (int c = 0; c < Cfg::EPI_COLS; c += 32) {
                         uint32_t v[32];
@@ -449,10 +623,17 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                             __syncwarp();
                             if (lane == 0) release_acc<Cfg>(&acc_empty[ab]);
                         }
+                        if (!ok) continue;
+                        if (role == 1) {
+                            slab.put(c, v);
+                            continue;
+                        }
+                        if (role == 2) slab.reduce_f32(c, v);
                         if (in_range)
                             store_block32<Cfg::STAGE_BUFS>(args, &tmap_c, next_buf(), m_base, n0 + col0 + c, v, true,
                                           tma_path);
                     }
+                    if (role == 1) slab.publish();
                     ++gr;
                 } else {
                     // K == 0: C = beta * C, tensor memory is never read
@@ -503,6 +684,14 @@ static cudaError_t launch_tc(const P &p, cudaStream_t stream) {
     a.C = p.C;
     a.ldc = p.ldc;
     a.c_tma = p.tmap_c != nullptr ? 1 : 0;
+    const TileSchedule &sc = p.sched;
+    a.num_units = static_cast<int>(sc.units);
+    a.split_tiles = static_cast<int>(sc.split_tiles);
+    a.split_parts = sc.parts;
+    a.split_gran = sc.gran;
+    a.split_q = sc.q;
+    a.partials = sc.partials;
+    a.counters = sc.counters;
     const CUtensorMap &tc = p.tmap_c != nullptr ? *p.tmap_c : *p.tmap_a;
     // After a pre-pass of this call, launch with programmatic stream
     // serialisation: the prologue overlaps the pre-pass's tail, and every
@@ -519,33 +708,48 @@ static cudaError_t launch_tc(const P &p, cudaStream_t stream) {
     lc.dynamicSmemBytes = Cfg::SMEM_BYTES;
     lc.stream = stream;
     lc.attrs = attr;
-    if constexpr (Cfg::CM == 1) {
-        const int tiles = a.num_m_tiles * a.num_n_tiles;
-        const int per_sm = p.blocks_per_sm < Cfg::MAX_BLOCKS ? p.blocks_per_sm : Cfg::MAX_BLOCKS;
-        int grid = p.sm_count * (per_sm > 0 ? per_sm : 1);
-        if (grid > tiles) grid = tiles;
-        if (grid < 1) return cudaSuccess;
-        lc.gridDim = dim3(grid);
-        lc.numAttrs = nattr;
-        return cudaLaunchKernelEx(&lc, tc_gemm_kernel<Cfg>, *p.tmap_a, *p.tmap_b, tc, a, p.ctx);
-    } else {
-        // clusters of CM CTAs; as many as can be resident at once (persistent)
-        const int sched_tiles = ((a.num_m_tiles + Cfg::CM - 1) / Cfg::CM) * a.num_n_tiles;
+    // one CTA (or CTA pair) per schedule slot, at most one per work unit
+    const long long units = sc.units;
+    const int grid_units = static_cast<int>(units < sc.slots ? units : sc.slots);
+    if (grid_units < 1) return cudaSuccess;
+    lc.gridDim = dim3(Cfg::CM * grid_units);
+    if constexpr (Cfg::CM > 1) {
         attr[nattr].id = cudaLaunchAttributeClusterDimension;
         attr[nattr].val.clusterDim.x = Cfg::CM;
         attr[nattr].val.clusterDim.y = 1;
         attr[nattr].val.clusterDim.z = 1;
         ++nattr;
-        lc.numAttrs = nattr;
-        int clusters = 0;
+    }
+    lc.numAttrs = nattr;
+    return cudaLaunchKernelEx(&lc, tc_gemm_kernel<Cfg>, *p.tmap_a, *p.tmap_b, tc, a, p.ctx);
+}
+
+// Schedule slots of a persistent launch: resident CTAs (at most MAX_BLOCKS per
+// SM, the TMEM limit), or resident clusters for a CTA pair.
+template <class Cfg>
+static cudaError_t tc_slots(const LaunchCommon &p, int *slots) {
+    if constexpr (Cfg::CM == 1) {
+        const int per_sm = p.blocks_per_sm < Cfg::MAX_BLOCKS ? p.blocks_per_sm : Cfg::MAX_BLOCKS;
+        *slots = p.sm_count * (per_sm > 0 ? per_sm : 1);
+        return cudaSuccess;
+    } else {
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = Cfg::CM;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cudaLaunchConfig_t lc{};
+        lc.blockDim = dim3(Cfg::THREADS);
+        lc.dynamicSmemBytes = Cfg::SMEM_BYTES;
         lc.gridDim = dim3(Cfg::CM * p.sm_count);
+        lc.attrs = attr;
+        lc.numAttrs = 1;
+        int clusters = 0;
         cudaError_t e = cudaOccupancyMaxActiveClusters(&clusters, tc_gemm_kernel<Cfg>, &lc);
         if (e != cudaSuccess) return e;
         if (clusters < 1) return cudaErrorInvalidConfiguration;
-        if (clusters > sched_tiles) clusters = sched_tiles;
-        if (clusters < 1) return cudaSuccess;
-        lc.gridDim = dim3(Cfg::CM * clusters);
-        return cudaLaunchKernelEx(&lc, tc_gemm_kernel<Cfg>, *p.tmap_a, *p.tmap_b, tc, a, p.ctx);
+        *slots = clusters;
+        return cudaSuccess;
     }
 }
 
@@ -564,6 +768,9 @@ static KernelInfo tc_info() {
     k.b_box_y = Cfg::BK;
     k.a_swizzle128 = k.b_swizzle128 = true;
     k.c_tma = true;
+    k.kc = Cfg::KC;
+    k.slabs_per_tile = Cfg::CM * Cfg::EPI;
+    k.schedule_slots = tc_slots<Cfg>;
     k.func = reinterpret_cast<const void *>(tc_gemm_kernel<Cfg>);
     return k;
 }
