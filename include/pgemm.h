@@ -73,6 +73,21 @@ typedef enum {
 /* Data types, for the introspection calls. */
 typedef enum { PGEMM_F32 = 0, PGEMM_BF16 = 1, PGEMM_I8 = 2 } pgemm_dtype;
 
+/* Who fills the shared-memory stages (pgemm_config.producer).
+ *   PGEMM_PRODUCER_TMA: TMA bulk-tensor copies into an S-stage ring guarded by
+ *     full / empty mbarriers, issued by one producer thread (every dtype; the
+ *     default).
+ *   PGEMM_PRODUCER_REGISTERS (fp32 only, stages = 2): the comparator of
+ *     "GPU-Kernel pipelinen" (step 3, the LDG-register variant) and of the
+ *     double-buffered SGEMM of "Double Buffering: Software Pipelining the
+ *     K-Loop" (section "The Kernel"): every thread of the block loads its
+ *     share of K-tile t+1 from global memory into registers while the block
+ *     computes tile t from one of two shared-memory buffers, then stores the
+ *     registers into the other buffer, and one block barrier per K-tile hands
+ *     the buffers over.  Same tile, register tile and arithmetic as the TMA
+ *     kernel; only the producer differs. */
+typedef enum { PGEMM_PRODUCER_TMA = 0, PGEMM_PRODUCER_REGISTERS = 1 } pgemm_producer;
+
 /* A kernel configuration: output tile bm x bn, K-tile bk (elements), and the
  * number of pipeline stages (shared-memory ring slots).  Stage count trades
  * latency coverage against shared memory and resident blocks ("Software
@@ -91,6 +106,7 @@ typedef enum { PGEMM_F32 = 0, PGEMM_BF16 = 1, PGEMM_I8 = 2 } pgemm_dtype;
 typedef struct {
     int bm, bn, bk, stages;
     int max_k_parts;
+    int producer; /* a pgemm_producer */
 } pgemm_config;
 
 /* fp32: FFMA register-tiled consumers on the pipelined ring.  Semantics are

@@ -187,7 +187,7 @@ static const KernelInfo *find_kernel(pgemm_dtype dt, const pgemm_config &c) {
     const KernelInfo *t = table_of(dt, &n);
     for (int i = 0; i < n; ++i)
         if (t[i].bm == c.bm && t[i].bn == c.bn && t[i].stages == c.stages &&
-            (c.bk == 0 || c.bk == t[i].bk))
+            (c.bk == 0 || c.bk == t[i].bk) && t[i].producer == c.producer)
             return &t[i];
     return nullptr;
 }
@@ -427,6 +427,7 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
         p.M = M; p.N = N; p.K = K; p.ldc = N; p.group_m = 0;
         p.sm_count = d->sm_count; p.blocks_per_sm = blocks_per_sm;
         p.tmap_a = &ta; p.tmap_b = &tb; p.tmap_c = tmap_c; p.ctx = ctx;
+        p.a_ptr = a_op; p.b_ptr = b_op; p.lda = a_ld; p.ldb = b_ld;
         p.after_prepass = after_prepass;
         p.alpha = alpha; p.beta = beta; p.C = C;
         e = k->launch_f32(p, stream);
@@ -435,6 +436,7 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
         p.M = M; p.N = N; p.K = K; p.ldc = N; p.group_m = 0;
         p.sm_count = d->sm_count; p.blocks_per_sm = blocks_per_sm;
         p.tmap_a = &ta; p.tmap_b = &tb; p.tmap_c = tmap_c; p.ctx = ctx;
+        p.a_ptr = a_op; p.b_ptr = b_op; p.lda = a_ld; p.ldb = b_ld;
         p.after_prepass = after_prepass;
         p.sched = sched;
         p.alpha = alpha; p.beta = beta; p.C = C;
@@ -444,6 +446,7 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
         p.M = M; p.N = N; p.K = K; p.ldc = N; p.group_m = 0;
         p.sm_count = d->sm_count; p.blocks_per_sm = blocks_per_sm;
         p.tmap_a = &ta; p.tmap_b = &tb; p.tmap_c = tmap_c; p.ctx = ctx;
+        p.a_ptr = a_op; p.b_ptr = b_op; p.lda = a_ld; p.ldb = b_ld;
         p.after_prepass = after_prepass;
         p.sched = sched;
         p.alpha = alpha; p.beta = beta; p.C = C;
@@ -525,7 +528,7 @@ pgemm_status pgemm_default_config(pgemm_dtype dtype, int M, int N, int K, pgemm_
 int pgemm_list_configs(pgemm_dtype dtype, pgemm_config *out, int cap) {
     int n = 0;
     const KernelInfo *t = table_of(dtype, &n);
-    for (int i = 0; i < n && i < cap && out; ++i) out[i] = pgemm_config{t[i].bm, t[i].bn, t[i].bk, t[i].stages, 0};
+    for (int i = 0; i < n && i < cap && out; ++i) out[i] = pgemm_config{t[i].bm, t[i].bn, t[i].bk, t[i].stages, 0, t[i].producer};
     return n;
 }
 

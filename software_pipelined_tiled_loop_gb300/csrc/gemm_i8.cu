@@ -67,27 +67,55 @@ struct WidenJob {
 };
 
 // dst[r][c] = (fp16) src[r][c] for r < rows, c < cols, for the two operands
-// (blockIdx.y selects A or B).  Vector path: each thread converts groups of 8
-// values (an 8-byte load, a 16-byte store), consecutive threads taking
-// consecutive groups, so every warp load and store is one contiguous run.
-__global__ void __launch_bounds__(256) widen_i8_to_f16_kernel(WidenJob ja, WidenJob jb) {
+// (blockIdx.y selects A or B).  Vector path: a block takes kWidenRows rows at
+// a time; its threads walk the rows' 8-value groups (an 8-byte load, a
+// 16-byte store each; consecutive lanes take consecutive groups, so every
+// warp store is 512 contiguous bytes of whole sectors).  Each thread loads
+// kWidenGroups groups of every row before converting any, keeping
+// kWidenRows * kWidenGroups independent loads in flight: one dependent load
+// per thread at a time covers only a fraction of the latency-bandwidth
+// product.  The fp16 output is written back through L2, where the GEMM that
+// follows finds most of it.
+constexpr int kWidenRows = 2;
+constexpr int kWidenGroups = 2;
+
+__global__ void __launch_bounds__(256, 6) widen_i8_to_f16_kernel(WidenJob ja, WidenJob jb) {
     const WidenJob &j = blockIdx.y == 0 ? ja : jb;
     if (j.rows <= 0 || j.cols <= 0) return;
-    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-    const long long t0 = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
     if (j.vec) {
-        const int per_row = j.cols / 8;  // cols % 16 == 0 on this path
-        const long long total = static_cast<long long>(per_row) * j.rows;
-        for (long long i = t0; i < total; i += stride) {
-            const long long r = i / per_row;
-            const int c0 = static_cast<int>(i - r * per_row) * 8;
-            const uint2 w = *reinterpret_cast<const uint2 *>(j.src + r * j.sld + c0);
-            __half2 o[4];
-            widen4(w.x, o[0], o[1]);
-            widen4(w.y, o[2], o[3]);
-            *reinterpret_cast<uint4 *>(j.dst + r * j.dld + c0) = *reinterpret_cast<const uint4 *>(o);
+        const int groups = j.cols / 8;  // cols % 16 == 0 on this path
+        const int step = static_cast<int>(blockDim.x) * kWidenGroups;
+        for (long long r0 = static_cast<long long>(blockIdx.x) * kWidenRows; r0 < j.rows;
+             r0 += static_cast<long long>(gridDim.x) * kWidenRows) {
+            const int nr = j.rows - r0 < kWidenRows ? static_cast<int>(j.rows - r0) : kWidenRows;
+            for (int c0 = threadIdx.x; c0 < groups; c0 += step) {
+                uint2 w[kWidenRows][kWidenGroups];
+#pragma unroll
+                for (int u = 0; u < kWidenRows; ++u)
+#pragma unroll
+                    for (int h = 0; h < kWidenGroups; ++h) {
+                        const int c = c0 + h * static_cast<int>(blockDim.x);
+                        if (u < nr && c < groups)
+                            w[u][h] = __ldg(reinterpret_cast<const uint2 *>(j.src + (r0 + u) * j.sld) + c);
+                    }
+#pragma unroll
+                for (int u = 0; u < kWidenRows; ++u)
+#pragma unroll
+                    for (int h = 0; h < kWidenGroups; ++h) {
+                        const int c = c0 + h * static_cast<int>(blockDim.x);
+                        if (u < nr && c < groups) {
+                            __half2 o[4];
+                            widen4(w[u][h].x, o[0], o[1]);
+                            widen4(w[u][h].y, o[2], o[3]);
+                            reinterpret_cast<uint4 *>(j.dst + (r0 + u) * j.dld)[c] =
+                                *reinterpret_cast<const uint4 *>(o);
+                        }
+                    }
+            }
         }
     } else {
+        const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+        const long long t0 = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
         const long long total = static_cast<long long>(j.rows) * j.cols;
         for (long long i = t0; i < total; i += stride) {
             const long long r = i / j.cols, c = i - r * j.cols;
@@ -113,12 +141,13 @@ cudaError_t launch_widen_i8_pair(const int8_t *a, long long lda, void *a_dst, lo
                                  int sm_count, cudaStream_t stream) {
     const WidenJob ja = make_job(a, lda, a_dst, a_dld, a_rows, a_cols);
     const WidenJob jb = make_job(b, ldb, b_dst, b_dld, b_rows, b_cols);
-    auto work = [](const WidenJob &j) -> long long {
-        return j.vec ? static_cast<long long>(j.cols / 8) * j.rows
-                     : static_cast<long long>(j.rows) * j.cols;
+    // vector path: one block per kWidenRows rows; scalar path: about four
+    // values per thread
+    auto blocks_for = [](const WidenJob &j) -> long long {
+        return j.vec ? (static_cast<long long>(j.rows) + kWidenRows - 1) / kWidenRows
+                     : (static_cast<long long>(j.rows) * j.cols + 1023) / 1024;
     };
-    long long items = work(ja) > work(jb) ? work(ja) : work(jb);
-    long long blocks = (items + 1023) / 1024;  // about four groups per thread
+    long long blocks = blocks_for(ja) > blocks_for(jb) ? blocks_for(ja) : blocks_for(jb);
     const long long cap = static_cast<long long>(sm_count) * 16;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;

@@ -53,6 +53,11 @@ struct LaunchCommon {
     bool after_prepass;         // a widening / repack kernel of this call precedes the GEMM
     KernelCtx ctx;
     TileSchedule sched;         // tensor-core kernels only
+    // The operands as the kernels read them (after any repack / widening):
+    // base pointers and pitches in elements, rows 16-byte aligned.  Used by
+    // kernels whose threads load the operands themselves.
+    const void *a_ptr, *b_ptr;
+    long long lda, ldb;
 };
 
 struct LaunchBf16 : LaunchCommon {
@@ -78,6 +83,7 @@ struct KernelInfo {
     int a_box_x = 0, a_box_y = 0, b_box_x = 0, b_box_y = 0;
     bool a_swizzle128 = true, b_swizzle128 = true;
     bool c_tma = false;  // the kernel can store C through a tensor map
+    int producer = PGEMM_PRODUCER_TMA;
     // Persistent tensor-core kernels: K-tiles per accumulation round (0 = all
     // of K) and the number of schedule slots (resident CTAs or CTA pairs) for
     // a launch; nullptr for the fp32 kernels, which do not split K.

@@ -59,6 +59,10 @@ def test_list_configs(L):
     # 128 x 256 single-CTA tiles fit four stages; the CTA pair's 256 x 256 six
     assert {c[3] for c in bf16 if c[1] == 256 and c[0] == 128} == {1, 2, 3, 4}
     assert {c[3] for c in bf16 if c[0] == 256} == {4, 5, 6}
+    # the register-staged comparator: fp32 only, two buffers, named by its producer
+    regs = [c for c in f32 if len(c) == 6 and c[5] == pg.PRODUCERS["registers"]]
+    assert {(c[0], c[1], c[3]) for c in regs} == {(128, 128, 2), (128, 64, 2)}
+    assert not [c for c in bf16 + i8 if len(c) == 6]
 
 
 @pytest.mark.parametrize("fn", ["gemm_f32", "gemm_bf16", "gemm_i8"])

@@ -128,13 +128,14 @@ def _configs(dtype):
 def test_every_config_every_tile_count(orc, dtype):
     """For every built (tile, S): K-tile counts T = 1, S-1, S, S+1, 2S+1 plus a
     K tail; shapes of several tiles in M and N with ragged edges."""
-    for (bm, bn, bk, S) in _configs(dtype):
+    for cfg in _configs(dtype):
+        bm, bn, bk, S = cfg[:4]
         for T in sorted({1, max(S - 1, 1), S, S + 1, 2 * S + 1}):
             for K in (T * bk, T * bk - bk // 2 if T > 1 else bk - 3):
                 M, N = 2 * bm + 7, 2 * bn + 24
                 kind = "random" if dtype == "i8" else "int"
                 check(orc, dtype, M, N, K, 1, 0, seed=7000 + 13 * S + T + K, kind=kind,
-                      config=(bm, bn, bk, S))
+                      config=cfg)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32", "i8"])
