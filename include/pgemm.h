@@ -88,6 +88,16 @@ typedef enum { PGEMM_F32 = 0, PGEMM_BF16 = 1, PGEMM_I8 = 2 } pgemm_dtype;
  *     kernel; only the producer differs. */
 typedef enum { PGEMM_PRODUCER_TMA = 0, PGEMM_PRODUCER_REGISTERS = 1 } pgemm_producer;
 
+/* Which multiply-accumulate consumes the stages (pgemm_config.engine).
+ *   PGEMM_ENGINE_DEFAULT: FFMA register tiles (fp32), tcgen05.mma into
+ *     tensor memory (bf16; int8 as exact fp16 products).
+ *   PGEMM_ENGINE_MMA_SYNC (int8 only): the alternative exact int8 route,
+ *     warp-level mma.sync.m16n8k32 s8 x s8 -> s32 on the int8 operands
+ *     themselves, 128 x 128 tiles, K-tiles of 128, on the same TMA ring (a
+ *     pre-pass writes B transposed, K-major, as the MMA's column operand
+ *     wants it).  Same results as the default, bit for bit. */
+typedef enum { PGEMM_ENGINE_DEFAULT = 0, PGEMM_ENGINE_MMA_SYNC = 1 } pgemm_engine;
+
 /* A kernel configuration: output tile bm x bn, K-tile bk (elements), and the
  * number of pipeline stages (shared-memory ring slots).  Stage count trades
  * latency coverage against shared memory and resident blocks ("Software
@@ -107,6 +117,7 @@ typedef struct {
     int bm, bn, bk, stages;
     int max_k_parts;
     int producer; /* a pgemm_producer */
+    int engine;   /* a pgemm_engine */
 } pgemm_config;
 
 /* fp32: FFMA register-tiled consumers on the pipelined ring.  Semantics are

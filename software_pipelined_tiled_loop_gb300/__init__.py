@@ -21,7 +21,7 @@ __all__ = [
     "pgemm_kernel_attrs", "pgemm_get_device_status", "pgemm_selftest_wait_timeout",
     "pgemm_status_string", "pgemm_version", "gemm_i8_noalloc", "NOALLOC_SCRATCH_BYTES",
     "pgemm_stage_reuse_demo", "pgemm_schedule", "pgemm_split_plan",
-    "DTYPES", "STATUS", "EXPORTED", "PRODUCERS",
+    "DTYPES", "STATUS", "EXPORTED", "PRODUCERS", "ENGINES",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -37,6 +37,8 @@ NOALLOC_SCRATCH_BYTES = 32 << 20
 DTYPES = {"f32": 0, "bf16": 1, "i8": 2}
 # pgemm_producer: who fills the shared-memory stages
 PRODUCERS = {"tma": 0, "registers": 1}
+# pgemm_engine: which multiply-accumulate consumes the stages
+ENGINES = {"default": 0, "mma_sync": 1}
 # Every function include/pgemm.h declares.
 EXPORTED = [
     "gemm_f32", "gemm_bf16", "gemm_i8", "gemm_f32_ex", "gemm_bf16_ex", "gemm_i8_ex",
@@ -56,17 +58,19 @@ class PgemmError(RuntimeError):
 
 
 class Config(ctypes.Structure):
-    """pgemm_config.  A tuple (bm, bn, bk, stages[, max_k_parts[, producer]])
-    converts to it."""
+    """pgemm_config.  A tuple (bm, bn, bk, stages[, max_k_parts[, producer[,
+    engine]]]) converts to it."""
     _fields_ = [("bm", ctypes.c_int), ("bn", ctypes.c_int), ("bk", ctypes.c_int),
                 ("stages", ctypes.c_int), ("max_k_parts", ctypes.c_int),
-                ("producer", ctypes.c_int)]
+                ("producer", ctypes.c_int), ("engine", ctypes.c_int)]
 
     def as_tuple(self):
         """The kernel the configuration names: (bm, bn, bk, stages), with
-        (..., max_k_parts, producer) appended for a non-TMA producer."""
-        if self.producer:
-            return (self.bm, self.bn, self.bk, self.stages, self.max_k_parts, self.producer)
+        (..., max_k_parts, producer, engine) appended when the producer or
+        the engine is not the default."""
+        if self.producer or self.engine:
+            return (self.bm, self.bn, self.bk, self.stages, self.max_k_parts, self.producer,
+                    self.engine)
         return (self.bm, self.bn, self.bk, self.stages)
 
 

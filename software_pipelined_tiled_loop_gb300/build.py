@@ -17,7 +17,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libpipegemm.so")
-SOURCES = ["api.cu", "gemm_f32.cu", "gemm_bf16.cu", "gemm_i8.cu", "gemm_i8_noalloc.cu",
+SOURCES = ["api.cu", "gemm_f32.cu", "gemm_bf16.cu", "gemm_i8.cu", "gemm_i8_imma.cu",
+           "gemm_i8_noalloc.cu",
            "stage_reuse.cu"]
 HEADERS = ["ptx.cuh", "common.cuh", "tc_gemm.cuh", "kernels.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

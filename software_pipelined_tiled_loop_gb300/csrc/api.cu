@@ -187,7 +187,8 @@ static const KernelInfo *find_kernel(pgemm_dtype dt, const pgemm_config &c) {
     const KernelInfo *t = table_of(dt, &n);
     for (int i = 0; i < n; ++i)
         if (t[i].bm == c.bm && t[i].bn == c.bn && t[i].stages == c.stages &&
-            (c.bk == 0 || c.bk == t[i].bk) && t[i].producer == c.producer)
+            (c.bk == 0 || c.bk == t[i].bk) && t[i].producer == c.producer &&
+            t[i].engine == c.engine)
             return &t[i];
     return nullptr;
 }
@@ -321,7 +322,10 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
     }
 
     // Operands as the kernels read them: element type, pitch, base pointer.
-    const int in_bytes = KIND == Kind::F32 ? 4 : 2;  // int8 is widened to fp16
+    // int8 is widened to fp16, except for the mma.sync engine, which reads
+    // the int8 values with B transposed (N rows of K).
+    const bool imma = KIND == Kind::I8 && k->engine == PGEMM_ENGINE_MMA_SYNC;
+    const int in_bytes = KIND == Kind::F32 ? 4 : (imma ? 1 : 2);
     const long long lda = K, ldb = N;
     const void *a_op = A;
     const void *b_op = B;
@@ -344,14 +348,16 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
     std::function<cudaError_t()> prepass;  // repack / widening launch, if any
     if (K > 0) {
         const long long align_elems = 16 / in_bytes;
-        const bool widen = KIND == Kind::I8;
+        const bool widen = KIND == Kind::I8 && !imma;
         const bool a_repack = widen || (lda * in_bytes) % 16 != 0;
-        const bool b_repack = widen || (ldb * in_bytes) % 16 != 0;
+        const bool b_repack = widen || imma || (ldb * in_bytes) % 16 != 0;
         if (a_repack || b_repack) {
             const long long a_ld2 = a_repack ? round_up(K, align_elems) : lda;
-            const long long b_ld2 = b_repack ? round_up(N, align_elems) : ldb;
+            const long long b_ld2 = imma ? round_up(K, align_elems)
+                                         : (b_repack ? round_up(N, align_elems) : ldb);
+            const long long b_rows = imma ? N : K;
             const long long a_bytes = a_repack ? round_up(a_ld2 * M * in_bytes, 256) : 0;
-            const long long b_bytes = b_repack ? round_up(b_ld2 * K * in_bytes, 256) : 0;
+            const long long b_bytes = b_repack ? round_up(b_ld2 * b_rows * in_bytes, 256) : 0;
             uint8_t *base = nullptr;
             if (fixed_scratch != nullptr) {
                 if (a_bytes + b_bytes > fixed_scratch_bytes) return PGEMM_ERR_TOO_LARGE;
@@ -364,6 +370,17 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
             // The pre-pass is launched below, after every tensor map is encoded,
             // so that the GEMM launch follows it with no host work in between.
             prepass = [=, &d]() -> cudaError_t {
+                if (imma) {  // A to a 16-byte pitch if needed; B -> B^T
+                    cudaError_t e = cudaSuccess;
+                    if (a_repack)
+                        e = launch_i8_relayout(reinterpret_cast<const int8_t *>(A), lda, base,
+                                               a_ld2, M, K, false, d->sm_count, stream);
+                    if (e == cudaSuccess)
+                        e = launch_i8_relayout(reinterpret_cast<const int8_t *>(B), ldb,
+                                               base + a_bytes, b_ld2, K, N, true, d->sm_count,
+                                               stream);
+                    return e;
+                }
                 if (widen)  // int8 -> fp16 of both operands in one launch
                     return launch_widen_i8_pair(reinterpret_cast<const int8_t *>(A), lda, base,
                                                 a_ld2, M, K, reinterpret_cast<const int8_t *>(B),
@@ -391,10 +408,15 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
     // Tensor maps.  With K == 0 nothing is ever loaded; the maps then describe
     // a 1 x 1 region of C so that they are still valid objects.
     alignas(64) CUtensorMap ta, tb;
-    const CUtensorMapDataType tmt = KIND == Kind::F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+    const CUtensorMapDataType tmt = KIND == Kind::F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                     : KIND == Kind::BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                    : imma               ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    if (K > 0) {
+    if (K > 0 && imma) {
+        st = encode_2d(&ta, tmt, 1, a_op, K, M, a_ld, k->a_box_x, k->a_box_y, k->a_swizzle128);
+        if (st == PGEMM_OK)  // B^T: N rows of K
+            st = encode_2d(&tb, tmt, 1, b_op, K, N, b_ld, k->b_box_x, k->b_box_y, k->b_swizzle128);
+    } else if (K > 0) {
         st = encode_2d(&ta, tmt, in_bytes, a_op, K, M, a_ld, k->a_box_x, k->a_box_y, k->a_swizzle128);
         if (st == PGEMM_OK)
             st = encode_2d(&tb, tmt, in_bytes, b_op, N, K, b_ld, k->b_box_x, k->b_box_y,
@@ -528,7 +550,7 @@ pgemm_status pgemm_default_config(pgemm_dtype dtype, int M, int N, int K, pgemm_
 int pgemm_list_configs(pgemm_dtype dtype, pgemm_config *out, int cap) {
     int n = 0;
     const KernelInfo *t = table_of(dtype, &n);
-    for (int i = 0; i < n && i < cap && out; ++i) out[i] = pgemm_config{t[i].bm, t[i].bn, t[i].bk, t[i].stages, 0, t[i].producer};
+    for (int i = 0; i < n && i < cap && out; ++i) out[i] = pgemm_config{t[i].bm, t[i].bn, t[i].bk, t[i].stages, 0, t[i].producer, t[i].engine};
     return n;
 }
 

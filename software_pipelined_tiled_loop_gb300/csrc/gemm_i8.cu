@@ -15,6 +15,8 @@
 // traffic through shared memory.
 #include <cuda_fp16.h>
 
+#include <vector>
+
 #include "tc_gemm.cuh"
 
 namespace pg {
@@ -35,14 +37,21 @@ static KernelInfo info_i8() {
 }
 
 const KernelInfo *i8_kernels(int *count) {
-    static const KernelInfo table[] = {
-        info_i8<256, 1>(), info_i8<256, 2>(), info_i8<256, 3>(), info_i8<256, 4>(),
-        info_i8<128, 2>(), info_i8<128, 3>(), info_i8<128, 4>(), info_i8<128, 5>(),
-        info_i8<128, 6>(), info_i8<128, 1>(),
-        info_i8<256, 4, 2>(), info_i8<256, 5, 2>(), info_i8<256, 6, 2>(),
-    };
-    *count = static_cast<int>(sizeof(table) / sizeof(table[0]));
-    return table;
+    // the exact-fp16 tcgen05 kernels, then the mma.sync engine's
+    static const std::vector<KernelInfo> table = [] {
+        std::vector<KernelInfo> t = {
+            info_i8<256, 1>(), info_i8<256, 2>(), info_i8<256, 3>(), info_i8<256, 4>(),
+            info_i8<128, 2>(), info_i8<128, 3>(), info_i8<128, 4>(), info_i8<128, 5>(),
+            info_i8<128, 6>(), info_i8<128, 1>(),
+            info_i8<256, 4, 2>(), info_i8<256, 5, 2>(), info_i8<256, 6, 2>(),
+        };
+        int n = 0;
+        const KernelInfo *imma = i8_imma_kernels(&n);
+        t.insert(t.end(), imma, imma + n);
+        return t;
+    }();
+    *count = static_cast<int>(table.size());
+    return table.data();
 }
 
 // Exact int8 -> fp16 for four packed bytes: bias each byte to b = x + 128,

@@ -84,6 +84,7 @@ struct KernelInfo {
     bool a_swizzle128 = true, b_swizzle128 = true;
     bool c_tma = false;  // the kernel can store C through a tensor map
     int producer = PGEMM_PRODUCER_TMA;
+    int engine = PGEMM_ENGINE_DEFAULT;
     // Persistent tensor-core kernels: K-tiles per accumulation round (0 = all
     // of K) and the number of schedule slots (resident CTAs or CTA pairs) for
     // a launch; nullptr for the fp32 kernels, which do not split K.
@@ -99,6 +100,7 @@ struct KernelInfo {
 const KernelInfo *bf16_kernels(int *count);
 const KernelInfo *f32_kernels(int *count);
 const KernelInfo *i8_kernels(int *count);
+const KernelInfo *i8_imma_kernels(int *count);  // gemm_i8_imma.cu (listed by i8_kernels)
 
 }  // namespace pg
 
@@ -109,6 +111,14 @@ cudaError_t launch_widen_i8_pair(const int8_t *a, long long lda, void *a_dst, lo
                                  int a_rows, int a_cols, const int8_t *b, long long ldb,
                                  void *b_dst, long long b_dld, int b_rows, int b_cols,
                                  int sm_count, cudaStream_t stream);
+}  // namespace pg
+
+namespace pg {
+// gemm_i8_imma.cu: dst = src or src^T for an int8 matrix (rows x cols, pitch
+// sld) into pitch dld; the operand pre-pass of the mma.sync int8 engine.
+cudaError_t launch_i8_relayout(const int8_t *src, long long sld, void *dst, long long dld,
+                               int rows, int cols, bool transpose, int sm_count,
+                               cudaStream_t stream);
 }  // namespace pg
 
 namespace pg {

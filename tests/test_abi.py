@@ -60,9 +60,14 @@ def test_list_configs(L):
     assert {c[3] for c in bf16 if c[1] == 256 and c[0] == 128} == {1, 2, 3, 4}
     assert {c[3] for c in bf16 if c[0] == 256} == {4, 5, 6}
     # the register-staged comparator: fp32 only, two buffers, named by its producer
-    regs = [c for c in f32 if len(c) == 6 and c[5] == pg.PRODUCERS["registers"]]
+    regs = [c for c in f32 if len(c) > 5 and c[5] == pg.PRODUCERS["registers"]]
     assert {(c[0], c[1], c[3]) for c in regs} == {(128, 128, 2), (128, 64, 2)}
-    assert not [c for c in bf16 + i8 if len(c) == 6]
+    assert not [c for c in bf16 + i8 if len(c) > 5 and c[5] != pg.PRODUCERS["tma"]]
+    # the mma.sync int8 engine: 128 x 128 tiles, K-tiles of 128 int8
+    imma = [c for c in i8 if len(c) > 6 and c[6] == pg.ENGINES["mma_sync"]]
+    assert {(c[0], c[1], c[2]) for c in imma} == {(128, 128, 128)}
+    assert {c[3] for c in imma} == {2, 3, 4, 6}
+    assert not [c for c in f32 + bf16 if len(c) > 6 and c[6] != pg.ENGINES["default"]]
 
 
 @pytest.mark.parametrize("fn", ["gemm_f32", "gemm_bf16", "gemm_i8"])

@@ -72,6 +72,8 @@ def check(orc, dtype, M, N, K, seed, kind="random", alpha=1, beta=0, config=None
 @pytest.mark.parametrize("dtype", ["bf16", "i8"])
 def test_every_config_splits_exactly(orc, dtype):
     for cfg in pg.pgemm_list_configs(dtype):
+        if len(cfg) > 4:  # another producer or engine: not a persistent tensor-core kernel
+            continue
         M, N, K = (300, 200, 4100) if cfg[0] == 256 else (250, 260, 4100)
         ok, s = splits(dtype, M, N, K, cfg)
         assert ok, (cfg, s)
