@@ -112,7 +112,10 @@ typedef enum { PGEMM_ENGINE_DEFAULT = 0, PGEMM_ENGINE_MMA_SYNC = 1 } pgemm_engin
  * and run first, side by side; the last part of a tile to finish adds the
  * others' partial sums (fp32, in part order, so the result does not depend
  * on timing; int8: exact int32) before the alpha/beta update.  max_k_parts =
- * 0: that choice; 1: never split; n > 1: at most n parts.  fp32 ignores it. */
+ * 0: that choice; 1: never split; n > 1: at most n parts.  fp32 (TMA
+ * producer) is persistent too and deals the leftover tiles' K-iterations out
+ * to every resident block instead (pgemm_stream_k_plan); max_k_parts = 1
+ * turns that off, other values leave it on. */
 typedef struct {
     int bm, bn, bk, stages;
     int max_k_parts;
@@ -199,8 +202,9 @@ PGEMM_API pgemm_status pgemm_kernel_attrs(pgemm_dtype dtype, const pgemm_config 
 /* The schedule a call with these arguments would use on the current device
  * (cfg NULL = default configuration): output tiles (a CTA pair's 256-row tile
  * counts once), schedule slots (units that run at once), tiles split along K
- * and their parts (0 and 1 when nothing is split).  No GPU work is enqueued.
- * Any output pointer may be NULL. */
+ * and their parts (0 and 1 when nothing is split; for fp32, the stream-K
+ * tiles and the most pieces one of them is spread over).  No GPU work is
+ * enqueued.  Any output pointer may be NULL. */
 PGEMM_API pgemm_status pgemm_schedule(pgemm_dtype dtype, const pgemm_config *cfg, int M, int N,
                                       int K, long long *tiles, int *slots,
                                       long long *split_tiles, int *parts);
@@ -217,6 +221,23 @@ PGEMM_API pgemm_status pgemm_schedule(pgemm_dtype dtype, const pgemm_config *cfg
 PGEMM_API pgemm_status pgemm_split_plan(long long tiles, int slots, int k_tiles, int round_tiles,
                                         int max_parts, long long *split_tiles, int *parts,
                                         int *gran, int *granules);
+
+/* The stream-K rule of the persistent fp32 kernels, a pure host computation
+ * (no device needed; the pages have no counterpart).  `tiles` output tiles on
+ * `slots` resident blocks with K of `k_tiles` K-tiles: when tiles % slots = R
+ * > 0, the R * k_tiles K-iterations of R tiles give every slot at least 8 and
+ * the longest share is at most 7/8 of k_tiles, those K-iterations are dealt
+ * out first, slot j taking iterations
+ * [j * R * k_tiles / slots, (j + 1) * R * k_tiles / slots) of the R tiles laid
+ * end to end; then each slot takes whole tiles R + j, R + j + slots, ...
+ * Outputs: R (0 when nothing is dealt out), the most slots any such tile is
+ * spread over (1 when none), and the K-iterations per slot.  The pieces of a
+ * tile each store their partial sums; the last to finish adds them in slot
+ * order (so results do not depend on timing) and writes C.  max_parts = 1
+ * turns it off (as pgemm_config.max_k_parts = 1 does for a call). */
+PGEMM_API pgemm_status pgemm_stream_k_plan(long long tiles, int slots, int k_tiles, int max_parts,
+                                           long long *sk_tiles, int *max_pieces,
+                                           long long *share);
 
 /* The stage-reuse hazard experiment of "Software pipelines and asynchronous
  * copies" (section "Practice"): a two-stage copy-and-reduce over the rows of

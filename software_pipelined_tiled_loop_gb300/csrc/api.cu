@@ -97,6 +97,12 @@ static pgemm_status kernel_setup(DeviceState &d, const KernelInfo &k, int *block
         if (cudaFuncSetAttribute(k.func, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  cudaSharedmemCarveoutMaxShared) != cudaSuccess)
             return PGEMM_ERR_CUDA;
+        if (k.aux_func != nullptr &&
+            (cudaFuncSetAttribute(k.aux_func, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  k.smem_bytes) != cudaSuccess ||
+             cudaFuncSetAttribute(k.aux_func, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  cudaSharedmemCarveoutMaxShared) != cudaSuccess))
+            return PGEMM_ERR_CUDA;
         int n = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k.func, k.threads, k.smem_bytes) !=
             cudaSuccess)
@@ -170,6 +176,18 @@ static TileSchedule plan_schedule(const KernelInfo &k, int M, int N, int K, int 
     s.units = s.tiles;
     if (k.schedule_slots == nullptr) return s;
     const int T = (K + k.bk - 1) / k.bk;
+    if (k.stream_k) {
+        long long share = 0;
+        if (pgemm_stream_k_plan(s.tiles, slots, T, max_parts, &s.split_tiles, &s.parts, &share) !=
+            PGEMM_OK)
+            return s;
+        if (s.split_tiles > 0) {
+            // a slot of partial sums for each of a slot's (at most two) pieces
+            s.partial_words = 2LL * slots * k.bm * k.bn;
+            s.counter_words = s.split_tiles;
+        }
+        return s;
+    }
     if (pgemm_split_plan(s.tiles, slots, T, k.kc, max_parts, &s.split_tiles, &s.parts, &s.gran,
                          &s.q) != PGEMM_OK)
         return s;
@@ -334,7 +352,7 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
     scratch.s = stream;
     Scratch split_area;  // partial sums and counters of K-split tiles
     split_area.s = stream;
-    if (sched.parts > 1) {
+    if (sched.split_tiles > 0) {
         const long long pbytes = round_up(sched.partial_words * 4, 256);
         const long long cbytes = round_up(sched.counter_words * 4, 256);
         if (cudaMallocAsync(&split_area.p, pbytes + cbytes, stream) != cudaSuccess)
@@ -451,6 +469,7 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
         p.tmap_a = &ta; p.tmap_b = &tb; p.tmap_c = tmap_c; p.ctx = ctx;
         p.a_ptr = a_op; p.b_ptr = b_op; p.lda = a_ld; p.ldb = b_ld;
         p.after_prepass = after_prepass;
+        p.sched = sched;
         p.alpha = alpha; p.beta = beta; p.C = C;
         e = k->launch_f32(p, stream);
     } else if constexpr (KIND == Kind::BF16) {
@@ -598,6 +617,42 @@ pgemm_status pgemm_split_plan(long long tiles, int slots, int k_tiles, int round
     if (p < 2) return PGEMM_OK;
     *parts = static_cast<int>(p);
     *split_tiles = rem;
+    return PGEMM_OK;
+}
+
+// The stream-K head of the persistent FFMA kernels: a piece of a tile is at
+// least kMinStreamKIters K-tiles, below which its exchange would cost about
+// what it saves, and the head is used only when its longest share is at most
+// 7/8 of a tile.
+constexpr long long kMinStreamKIters = 8;
+
+pgemm_status pgemm_stream_k_plan(long long tiles, int slots, int k_tiles, int max_parts,
+                                 long long *sk_tiles, int *max_pieces, long long *share) {
+    if (tiles < 0 || slots < 1 || k_tiles < 0 || max_parts < 0 || !sk_tiles || !max_pieces ||
+        !share)
+        return PGEMM_ERR_INVALID_VALUE;
+    *sk_tiles = 0;
+    *max_pieces = 1;
+    *share = 0;
+    if (max_parts == 1 || k_tiles == 0 || slots < 2) return PGEMM_OK;
+    const long long rem = tiles % slots;
+    if (rem == 0) return PGEMM_OK;
+    const long long total = rem * k_tiles;
+    if (total / slots < kMinStreamKIters) return PGEMM_OK;
+    // worth it only if the longest share saves at least an eighth of a tile
+    // over the extra wave it replaces
+    const long long longest = (total + slots - 1) / slots;
+    if (longest * 8 > static_cast<long long>(k_tiles) * 7) return PGEMM_OK;
+    // slot holding stream-K iteration x: the largest j with j * total / slots <= x
+    auto slot_of = [&](long long x) { return ((x + 1) * slots - 1) / total; };
+    long long most = 1;
+    for (long long r = 0; r < rem; ++r) {
+        const long long p = slot_of((r + 1) * k_tiles - 1) - slot_of(r * k_tiles) + 1;
+        if (p > most) most = p;
+    }
+    *sk_tiles = rem;
+    *max_pieces = static_cast<int>(most);
+    *share = total / slots;
     return PGEMM_OK;
 }
 

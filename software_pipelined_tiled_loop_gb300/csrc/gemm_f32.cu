@@ -116,43 +116,78 @@ __device__ __forceinline__ void mma_ktile(AccTile<BN> &acc, uint32_t a_base, uin
     }
 }
 
+// C[row][col .. col+3] as a float4 (zeros outside C): one 16-byte load where
+// the four columns are in range and aligned, else element by element.
+__device__ __forceinline__ float4 load_c4(const GemmArgs<float, float> &args, int row, int col) {
+    float4 c = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (row >= args.M || col >= args.N) return c;
+    const float *cp = args.C + static_cast<long long>(row) * args.ldc + col;
+    if (col + 4 <= args.N && (reinterpret_cast<uintptr_t>(cp) & 15u) == 0)
+        return *reinterpret_cast<const float4 *>(cp);
+    c.x = cp[0];
+    if (col + 1 < args.N) c.y = cp[1];
+    if (col + 2 < args.N) c.z = cp[2];
+    if (col + 3 < args.N) c.w = cp[3];
+    return c;
+}
+
+// C[row][col .. col+3] <- alpha * v + beta * c (c: the old C values, read
+// only when beta != 0), a 16-byte store where in range and aligned.
+__device__ __forceinline__ void put_c4(const GemmArgs<float, float> &args, int row, int col,
+                                       const float4 &v, const float4 &c) {
+    if (row >= args.M || col >= args.N) return;
+    float *cp = args.C + static_cast<long long>(row) * args.ldc + col;
+    float4 o;
+    if (args.beta != 0.f)
+        o = make_float4(axpby(args.alpha, v.x, args.beta, c.x), axpby(args.alpha, v.y, args.beta, c.y),
+                        axpby(args.alpha, v.z, args.beta, c.z), axpby(args.alpha, v.w, args.beta, c.w));
+    else
+        o = make_float4(args.alpha * v.x, args.alpha * v.y, args.alpha * v.z, args.alpha * v.w);
+    if (col + 4 <= args.N && (reinterpret_cast<uintptr_t>(cp) & 15u) == 0) {
+        *reinterpret_cast<float4 *>(cp) = o;
+    } else {
+        cp[0] = o.x;
+        if (col + 1 < args.N) cp[1] = o.y;
+        if (col + 2 < args.N) cp[2] = o.z;
+        if (col + 3 < args.N) cp[3] = o.w;
+    }
+}
+
+// The thread's float4 f = i * (BN/32) + k of a tile holds row 8*i + tr,
+// columns 16*k + 4*tc .. +3 of its warp tile.
+template <int BN>
+__device__ __forceinline__ void c4_coords(int f, int m0, int n0, int wm, int wn, int tr, int tc,
+                                          int &row, int &col) {
+    row = m0 + wm * 64 + 8 * (f / (BN / 32)) + tr;
+    col = n0 + wn * (BN / 2) + 16 * (f % (BN / 32)) + 4 * tc;
+}
+
 // C <- alpha * acc + beta * C for this thread's part of the tile at (m0, n0).
+// With beta != 0 the old C values are read eight float4 at a time, all eight
+// loads in flight before the first store, instead of one round trip each.
 template <int BN>
 __device__ __forceinline__ void store_tile(const GemmArgs<float, float> &args, const AccTile<BN> &acc,
                                            int m0, int n0, int wm, int wn, int tr, int tc) {
-    constexpr int G = BN / 32, WN = BN / 2;
+    constexpr int NF = 8 * (BN / 32);
     const bool read_c = args.beta != 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int row = m0 + wm * 64 + 8 * i + tr;
-        if (row >= args.M) continue;
-        float *crow = args.C + static_cast<long long>(row) * args.ldc;
+    for (int f0 = 0; f0 < NF; f0 += 8) {
+        float4 c[8];
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-            const int col = n0 + wn * WN + 16 * g + 4 * tc;
-            float *cp = crow + col;
-            const float v[4] = {acc[i][2 * g].x, acc[i][2 * g].y, acc[i][2 * g + 1].x,
-                                acc[i][2 * g + 1].y};
-            if (col + 4 <= args.N && (reinterpret_cast<uintptr_t>(cp) & 15u) == 0) {
-                float4 o;
-                if (read_c) {
-                    const float4 c = *reinterpret_cast<const float4 *>(cp);
-                    o = make_float4(axpby(args.alpha, v[0], args.beta, c.x),
-                                    axpby(args.alpha, v[1], args.beta, c.y),
-                                    axpby(args.alpha, v[2], args.beta, c.z),
-                                    axpby(args.alpha, v[3], args.beta, c.w));
-                } else {
-                    o = make_float4(args.alpha * v[0], args.alpha * v[1], args.alpha * v[2],
-                                    args.alpha * v[3]);
-                }
-                *reinterpret_cast<float4 *>(cp) = o;
-            } else {
+        for (int e = 0; e < 8; ++e) {
+            int row, col;
+            c4_coords<BN>(f0 + e, m0, n0, wm, wn, tr, tc, row, col);
+            c[e] = read_c ? load_c4(args, row, col) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    if (col + e < args.N)
-                        cp[e] = read_c ? axpby(args.alpha, v[e], args.beta, cp[e])
-                                       : args.alpha * v[e];
-            }
+        for (int e = 0; e < 8; ++e) {
+            const int f = f0 + e, i = f / (BN / 32), k = f % (BN / 32);
+            int row, col;
+            c4_coords<BN>(f, m0, n0, wm, wn, tr, tc, row, col);
+            put_c4(args, row, col,
+                   make_float4(acc[i][2 * k].x, acc[i][2 * k].y, acc[i][2 * k + 1].x,
+                               acc[i][2 * k + 1].y),
+                   c[e]);
         }
     }
 }
@@ -186,8 +221,13 @@ __global__ void __launch_bounds__(128, F32Cfg<BN_, STAGES>::MIN_BLOCKS)
     }
     __syncthreads();
 
+    // A stream-K tail grid behind this one may start once every block of this
+    // grid has started: its blocks then take over the slots these free.
+    grid_launch_dependents();
+    // whole tiles follow the stream-K tiles [0, args.split_tiles)
     int m0, n0;
-    tile_origin(blockIdx.x, args.num_m_tiles, args.num_n_tiles, args.group_m, BM, BN, m0, n0);
+    tile_origin(static_cast<int>(blockIdx.x) + args.split_tiles, args.num_m_tiles,
+                args.num_n_tiles, args.group_m, BM, BN, m0, n0);
     const int T = args.num_k_tiles;
     const bool producer = threadIdx.x == 0;
 
@@ -253,6 +293,243 @@ __global__ void __launch_bounds__(128, F32Cfg<BN_, STAGES>::MIN_BLOCKS)
 
     // ---------------- epilogue: alpha * acc + beta * C ----------------
     store_tile<BN>(args, acc, m0, n0, wm, wn, tr, tc);
+}
+
+// The stream-K tail (args.split_tiles = R > 0 output tiles, the tiles the
+// full waves would leave over): the whole tiles [R, tiles), exactly full
+// waves, run first in gemm_f32_kernel; this grid of G blocks, one per
+// resident slot, is launched behind it with programmatic serialisation, so
+// its blocks take over each SM slot a whole-tile block frees.  It deals the
+// R * T K-iterations of tiles [0, R) out in equal contiguous ranges, block j
+// taking [j * R * T / G, (j + 1) * R * T / G) (pieces of at most two tiles,
+// since R < G): the leftover tiles cost R / G of a tile per slot instead of a
+// whole extra wave.  (Run first instead, the two blocks sharing an SM end
+// their equal shares at different times, and the whole tiles behind them
+// end staggered by as much.)  A piece ends in an exchange: every
+// piece stores its raw partial sums to its own slot in `partials`, counts
+// itself on the tile's ticket in `counters` (after a fence), and the piece
+// that takes the last ticket adds all pieces in slot order (so the result
+// does not depend on timing) and writes C.  Nothing waits on another block.
+struct F32Stream {
+    int T, G, j, R;
+    long long sk_a, sk_total;
+    int sk_len, n_sk;
+
+    __device__ __forceinline__ void init(const GemmArgs<float, float> &a) {
+        T = a.num_k_tiles;
+        G = static_cast<int>(gridDim.x);
+        j = static_cast<int>(blockIdx.x);
+        R = a.split_tiles;
+        sk_total = static_cast<long long>(R) * T;
+        sk_a = R > 0 ? j * sk_total / G : 0;
+        sk_len = R > 0 ? static_cast<int>((j + 1) * sk_total / G - sk_a) : 0;
+        n_sk = sk_len == 0 ? 0 : ((sk_a / T) == ((sk_a + sk_len - 1) / T) ? 1 : 2);
+    }
+    __device__ __forceinline__ int units() const { return n_sk; }
+    __device__ __forceinline__ int iterations() const { return sk_len; }
+    // piece u (0 or 1): its tile and K-tiles [kb, ke)
+    __device__ __forceinline__ void unit(int u, int &tile, int &kb, int &ke) const {
+        tile = static_cast<int>(sk_a / T) + u;
+        const long long t0 = static_cast<long long>(tile) * T;
+        const long long lo = sk_a > t0 ? sk_a : t0;
+        const long long end = sk_a + sk_len, hi = end < t0 + T ? end : t0 + T;
+        kb = static_cast<int>(lo - t0);
+        ke = static_cast<int>(hi - t0);
+    }
+    // the slot holding stream-K iteration x
+    __device__ __forceinline__ int slot_of(long long x) const {
+        return static_cast<int>(((x + 1) * G - 1) / sk_total);
+    }
+};
+
+template <int BN_, int STAGES>
+__global__ void __launch_bounds__(128, F32Cfg<BN_, STAGES>::MIN_BLOCKS)
+    gemm_f32_streamk_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                            const __grid_constant__ CUtensorMap tmap_b,
+                            const GemmArgs<float, float> args, const KernelCtx ctx) {
+    using Cfg = F32Cfg<BN_, STAGES>;
+    constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align_1024(smem_raw);
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + STAGES * Cfg::A_BYTES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + Cfg::BAR_OFFSET);
+    uint64_t *empty = full + STAGES;
+    __shared__ int last_piece;
+    // The schedule and the producer's cursor (the unit and K-tile of its next
+    // load) live in shared memory: they are read once per unit or K-tile,
+    // and registers are all taken by the 8 x 16 tile.
+    __shared__ F32Stream ws;
+    __shared__ int pc[6];  // unit, tile, next K-tile, end K-tile, m0, n0
+
+    const uint32_t warp = warp_id_uniform();
+    const uint32_t lane = lane_id();
+    const int tid = static_cast<int>(threadIdx.x);
+
+    if (threadIdx.x == 0) {
+        prefetch_tmap(&tmap_a);
+        prefetch_tmap(&tmap_b);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], Cfg::CONSUMER_WARPS);
+        }
+        fence_barrier_init();
+        ws.init(args);
+    }
+    __syncthreads();
+
+    const int total = ws.iterations();
+    const int nunits = ws.units();
+    const bool producer = threadIdx.x == 0;
+
+    auto p_enter = [&](int u) {
+        int tile, kb, ke, m0, n0;
+        ws.unit(u, tile, kb, ke);
+        tile_origin(tile, args.num_m_tiles, args.num_n_tiles, args.group_m, BM, BN, m0, n0);
+        pc[0] = u;
+        pc[1] = tile;
+        pc[2] = kb;
+        pc[3] = ke;
+        pc[4] = m0;
+        pc[5] = n0;
+    };
+    // Issue the TMA copies of the next iteration (number g) into slot g % S.
+    auto issue = [&](int g) {
+        while (pc[2] == pc[3]) p_enter(pc[0] + 1);
+        const int s = g % STAGES, kt = pc[2];
+        mbar_arrive_expect_tx(&full[s], Cfg::STAGE_BYTES);
+        tma_load_2d(sA + s * Cfg::A_BYTES, &tmap_a, &full[s], kt * BK, pc[4]);
+        tma_load_2d(sB + s * Cfg::B_BYTES, &tmap_b, &full[s], pc[5], kt * BK);
+        pc[2] = kt + 1;
+    };
+    int next_load = 0;  // iterations [0, next_load) have been issued (producer lane only)
+    if (producer && total > 0) {
+        p_enter(0);
+        // prologue: fill min(S, total) slots
+        for (; next_load < total && next_load < STAGES; ++next_load) issue(next_load);
+    }
+
+    // ---------------- consumers ----------------
+    const int wm = static_cast<int>(warp) >> 1;  // warp tile row (0..1)
+    const int wn = static_cast<int>(warp) & 1;   // warp tile column (0..1)
+    const int tr = static_cast<int>(lane) >> 2;  // 0..7
+    const int tc = static_cast<int>(lane) & 3;   // 0..3
+
+    constexpr int WN = BN / 2;
+    // byte offsets inside a slot
+    const uint32_t a_row0 = static_cast<uint32_t>((wm * 64 + tr) * 128);  // row 8*i+tr: + i*1024
+    const uint32_t b_col0 = static_cast<uint32_t>((wn * WN + tc * 4) * 4);
+
+    // A failed (timed-out) wait is recorded and the block keeps going
+    // without waiting, so that every thread still meets every block barrier.
+    bool ok = true;
+    int g = 0;
+    for (int u = 0; u < nunits; ++u) {
+        int tile, kb, ke;
+        ws.unit(u, tile, kb, ke);
+        AccTile<BN> acc;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int k = 0; k < BN / 16; ++k) acc[i][k] = make_float2(0.f, 0.f);
+        for (int kt = kb; kt < ke; ++kt, ++g) {
+            if (producer && ok) {
+                // steady state: refill released slots, up to S iterations ahead of g
+                while (next_load < total && next_load < g + STAGES) {
+                    const int prev = next_load - STAGES;  // last iteration that used this slot
+                    uint64_t *e = &empty[next_load % STAGES];
+                    const uint32_t par = static_cast<uint32_t>(prev / STAGES) & 1u;
+                    if (!mbar_test_wait(e, par)) {
+                        if (next_load > g) break;  // not needed yet: try again next iteration
+                        if (!mbar_wait(e, par, ctx, kSiteProducerEmpty)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    issue(next_load++);
+                }
+            }
+            const uint32_t s = g % STAGES, ph = (g / STAGES) & 1u;
+            if (ok && !mbar_wait(&full[s], ph, ctx, kSiteConsumerFull)) ok = false;
+            const uint32_t a_base = smem_u32(sA + s * Cfg::A_BYTES) + a_row0;
+            const uint32_t b_base = smem_u32(sB + s * Cfg::B_BYTES) + b_col0;
+            mma_ktile<BN, 0, BK / 4>(acc, a_base, b_base, tr);
+            // Release the slot: this warp's reads of it are done.
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
+
+        int m0, n0;
+        tile_origin(tile, args.num_m_tiles, args.num_n_tiles, args.group_m, BM, BN, m0, n0);
+        // a piece of `tile`: leave the partial sums, take a ticket
+        const int first = ws.slot_of(static_cast<long long>(tile) * ws.T);
+        const int last = ws.slot_of(static_cast<long long>(tile + 1) * ws.T - 1);
+        float4 *mine = reinterpret_cast<float4 *>(args.partials) +
+                       static_cast<long long>(ws.j * 2 + u) * (BM * BN / 4);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int k = 0; k < BN / 32; ++k)
+                mine[(i * (BN / 32) + k) * 128 + tid] =
+                    make_float4(acc[i][2 * k].x, acc[i][2 * k].y, acc[i][2 * k + 1].x,
+                                acc[i][2 * k + 1].y);
+        __threadfence();
+        __syncthreads();
+        if (tid == 0)
+            last_piece = atomicAdd(&args.counters[tile], 1u) == static_cast<uint32_t>(last - first);
+        __syncthreads();
+        if (last_piece) {
+            __threadfence();
+            // Every piece is stored: add them in slot order straight into C
+            // (float4 f of each piece holds the same elements of the tile),
+            // eight float4 of C and of every piece in flight at once.
+            constexpr int NF = 8 * (BN / 32);
+            const bool read_c = args.beta != 0.f;
+#pragma unroll 1
+            for (int f0 = 0; f0 < NF; f0 += 8) {
+                float4 c[8], sum[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    int row, col;
+                    c4_coords<BN>(f0 + e, m0, n0, wm, wn, tr, tc, row, col);
+                    c[e] = read_c ? load_c4(args, row, col) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+                for (int q = first; q <= last; ++q) {
+                    const int qunit = tile - static_cast<int>(
+                                                 (static_cast<long long>(q) * ws.sk_total / ws.G) / ws.T);
+                    const float4 *src = reinterpret_cast<const float4 *>(args.partials) +
+                                        static_cast<long long>(q * 2 + qunit) * (BM * BN / 4) +
+                                        f0 * 128 + tid;
+                    float4 x[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) x[e] = __ldcg(src + e * 128);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        if (q == first) {
+                            sum[e] = x[e];
+                        } else {
+                            sum[e].x += x[e].x;
+                            sum[e].y += x[e].y;
+                            sum[e].z += x[e].z;
+                            sum[e].w += x[e].w;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    int row, col;
+                    c4_coords<BN>(f0 + e, m0, n0, wm, wn, tr, tc, row, col);
+                    if (ok) put_c4(args, row, col, sum[e], c[e]);
+                }
+            }
+        }
+        __syncthreads();  // last_piece is read by every thread before it is rewritten
+    }
+    // This grid runs beside the tail of the whole-tile grid launched before
+    // it; it does not end before that grid has, so that later work on the
+    // stream sees all of C.
+    grid_dependency_wait();
 }
 
 // ------------------------------------------- register-staged comparator ---
@@ -426,11 +703,39 @@ static cudaError_t launch_f32_impl(const LaunchF32 &p, cudaStream_t stream) {
     a.beta = p.beta;
     a.C = p.C;
     a.ldc = p.ldc;
-    const int tiles = a.num_m_tiles * a.num_n_tiles;
+    a.split_tiles = static_cast<int>(p.sched.split_tiles);
+    a.partials = p.sched.partials;
+    a.counters = p.sched.counters;
+    const long long tiles = static_cast<long long>(a.num_m_tiles) * a.num_n_tiles;
     if (tiles < 1) return cudaSuccess;
-    gemm_f32_kernel<BN, STAGES><<<tiles, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(
-        *p.tmap_a, *p.tmap_b, a, p.ctx);
-    return cudaGetLastError();
+    // the whole tiles, one block each
+    const long long whole = tiles - a.split_tiles;
+    if (whole > 0) {
+        gemm_f32_kernel<BN, STAGES><<<static_cast<unsigned>(whole), Cfg::THREADS,
+                                      Cfg::SMEM_BYTES, stream>>>(*p.tmap_a, *p.tmap_b, a, p.ctx);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess || a.split_tiles == 0) return e;
+    }
+    // the stream-K tail: one block per resident slot, programmatically
+    // serialised behind the whole tiles so that it fills the slots they free
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t lc{};
+    lc.gridDim = dim3(static_cast<unsigned>(p.sched.slots));
+    lc.blockDim = dim3(Cfg::THREADS);
+    lc.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    lc.stream = stream;
+    lc.attrs = attr;
+    lc.numAttrs = whole > 0 ? 1 : 0;
+    return cudaLaunchKernelEx(&lc, gemm_f32_streamk_kernel<BN, STAGES>, *p.tmap_a, *p.tmap_b, a,
+                              p.ctx);
+}
+
+template <int BN, int STAGES>
+static cudaError_t f32_slots(const LaunchCommon &p, int *slots) {
+    *slots = p.sm_count * (p.blocks_per_sm > 0 ? p.blocks_per_sm : 1);
+    return cudaSuccess;
 }
 
 template <int BN>
@@ -493,7 +798,10 @@ static KernelInfo info_f32() {
     k.b_box_y = Cfg::BK;
     k.a_swizzle128 = true;
     k.b_swizzle128 = false;
+    k.stream_k = true;
+    k.schedule_slots = f32_slots<BN, STAGES>;
     k.func = reinterpret_cast<const void *>(gemm_f32_kernel<BN, STAGES>);
+    k.aux_func = reinterpret_cast<const void *>(gemm_f32_streamk_kernel<BN, STAGES>);
     k.launch_f32 = launch_f32_impl<BN, STAGES>;
     return k;
 }

@@ -52,7 +52,7 @@ struct LaunchCommon {
     const CUtensorMap *tmap_c;  // C as a 32 x 32-box, 128-byte-swizzled map, or nullptr
     bool after_prepass;         // a widening / repack kernel of this call precedes the GEMM
     KernelCtx ctx;
-    TileSchedule sched;         // tensor-core kernels only
+    TileSchedule sched;         // persistent kernels only
     // The operands as the kernels read them (after any repack / widening):
     // base pointers and pitches in elements, rows 16-byte aligned.  Used by
     // kernels whose threads load the operands themselves.
@@ -85,13 +85,18 @@ struct KernelInfo {
     bool c_tma = false;  // the kernel can store C through a tensor map
     int producer = PGEMM_PRODUCER_TMA;
     int engine = PGEMM_ENGINE_DEFAULT;
-    // Persistent tensor-core kernels: K-tiles per accumulation round (0 = all
-    // of K) and the number of schedule slots (resident CTAs or CTA pairs) for
-    // a launch; nullptr for the fp32 kernels, which do not split K.
+    // Persistent kernels: K-tiles per accumulation round (0 = all of K) and
+    // the number of schedule slots (resident CTAs or CTA pairs) for a
+    // launch; nullptr for kernels with one block per tile.
     int kc = 0;
     int slabs_per_tile = 0;  // epilogue warps per tile (all CTAs of a pair)
+    // FFMA kernels: the leftover tiles' K-iterations are dealt out to all
+    // slots by a head grid (aux_func) before the whole tiles, instead of
+    // K-splitting whole tiles.
+    bool stream_k = false;
     cudaError_t (*schedule_slots)(const LaunchCommon &, int *slots) = nullptr;
     const void *func = nullptr;
+    const void *aux_func = nullptr;  // a second kernel of the same launch (same attributes)
     cudaError_t (*launch_bf16)(const LaunchBf16 &, cudaStream_t) = nullptr;
     cudaError_t (*launch_f32)(const LaunchF32 &, cudaStream_t) = nullptr;
     cudaError_t (*launch_i8)(const LaunchI8 &, cudaStream_t) = nullptr;

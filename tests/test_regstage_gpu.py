@@ -69,7 +69,8 @@ def test_regstage_equals_tma_kernel_bitwise(bn):
     M, N, K = 1000, 1000, 1000
     A, B, C = operands(M, N, K, 950, "random")
     a, st_a = run_gpu("f32", A, B, C, 1.0, 0.5, config=(128, bn, 32, 2, 0, REG))
-    b, st_b = run_gpu("f32", A, B, C, 1.0, 0.5, config=(128, bn, 32, 2))
+    # the TMA kernel without its stream-K head, which would add pieces in another order
+    b, st_b = run_gpu("f32", A, B, C, 1.0, 0.5, config=(128, bn, 32, 2, 1))
     assert st_a == 0 and st_b == 0
     assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
 

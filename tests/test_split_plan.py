@@ -105,3 +105,55 @@ def test_bench_shapes():
 def test_plan_rejects_bad_arguments(args):
     with pytest.raises(pg.PgemmError):
         pg.pgemm_split_plan(*args)
+
+
+# ------------------------------------------------ fp32 stream-K head ---------
+def sk_slot_ranges(R, T, G):
+    total = R * T
+    return [(j * total // G, (j + 1) * total // G) for j in range(G)]
+
+
+SK_CASES = list(itertools.product(
+    [1, 4, 100, 112, 303, 304, 305, 1024, 1100],   # tiles
+    [2, 76, 304],                                   # slots
+    [0, 1, 7, 8, 64, 128, 513],                     # K-tiles
+    [0, 1],                                         # max_k_parts
+))
+
+
+@pytest.mark.parametrize("tiles,slots,T,maxp", SK_CASES)
+def test_stream_k_plan_properties(tiles, slots, T, maxp):
+    p = pg.pgemm_stream_k_plan(tiles, slots, T, maxp)
+    R = tiles % slots
+    if p["sk_tiles"] == 0:
+        assert p["max_pieces"] == 1
+        # off only when a rule says so
+        assert (maxp == 1 or T == 0 or R == 0 or R * T // slots < 8
+                or 8 * -(-R * T // slots) > 7 * T)
+        return
+    assert maxp != 1 and p["sk_tiles"] == R and p["share"] == R * T // slots >= 8
+    ranges = sk_slot_ranges(R, T, slots)
+    # the slots' ranges tile the R * T iterations exactly, none is empty,
+    # and none spans more than two tiles (the kernel keeps two partial slots)
+    assert ranges[0][0] == 0 and ranges[-1][1] == R * T
+    assert all(b == c for (_, b), (c, _) in zip(ranges, ranges[1:]))
+    assert all(b > a and (b - 1) // T - a // T <= 1 for a, b in ranges)
+    # pieces per tile: the kernel's closed form agrees with the ranges
+    def slot_of(x):
+        return ((x + 1) * slots - 1) // (R * T)
+    most = 1
+    for r in range(R):
+        owners = [j for j, (a, b) in enumerate(ranges) if a < (r + 1) * T and b > r * T]
+        assert owners == list(range(slot_of(r * T), slot_of((r + 1) * T - 1) + 1))
+        most = max(most, len(owners))
+    assert p["max_pieces"] == most
+    # makespan in tile-times: W whole waves plus the largest share, below W + 1
+    W = tiles // slots
+    longest = max(b - a for a, b in ranges)
+    assert W + longest / T <= math.ceil(tiles / slots) - 1 / 8
+
+
+def test_stream_k_bench_shape():
+    # fp32 4096^3 on 152 SMs x 2 blocks: 1024 tiles, 112 left after three waves
+    p = pg.pgemm_stream_k_plan(1024, 304, 128)
+    assert p["sk_tiles"] == 112 and p["share"] == 112 * 128 // 304
