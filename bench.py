@@ -102,6 +102,27 @@ def traffic_for(kernel_key: str):
     return e.get("dram_bytes_per_launch")
 
 
+def launches_per_call(dtype: str, M: int, N: int, K: int) -> int:
+    """This library's kernel launches in one default call: the operand pre-pass
+    (int8 widening of A and B in one launch; a repack per bf16/fp32 operand
+    whose pitch is not a multiple of 16 bytes), then the GEMM, which for fp32
+    is two grids when the stream-K tail is in use."""
+    import software_pipelined_tiled_loop_gb300 as pg
+    eb = {"f32": 4, "bf16": 2, "i8": 1}[dtype]
+    n = 0
+    if K > 0:
+        if dtype == "i8":
+            n += 1
+        else:
+            n += int((K * eb) % 16 != 0) + int((N * eb) % 16 != 0)
+    s = pg.pgemm_schedule(dtype, M, N, K)
+    if dtype == "f32" and s["split_tiles"] > 0:
+        n += 1 + int(s["tiles"] > s["split_tiles"])
+    else:
+        n += 1
+    return n
+
+
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "software_pipelined_tiled_loop_gb300", "csrc")
@@ -237,7 +258,7 @@ def run_gpu_workload(name: str, steps: int, warmup: int, dist_ctx, with_e2e: boo
            "ms_median": statistics.median(per_step_ms),
            "tflops": aggregate_throughput(flops, steps, dist_ctx.world, total_ms),
            "per_gpu_tflops": flops * steps / (total_ms * 1e-3) / 1e12,
-           "launches_per_step": 1 if dtype != "i8" else 3,
+           "launches_per_step": launches_per_call(dtype, M, N, K),
            "config": pg.pgemm_default_config(dtype, M, N, K), "clocks": clk}
 
     if with_e2e:

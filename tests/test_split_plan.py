@@ -107,7 +107,7 @@ def test_plan_rejects_bad_arguments(args):
         pg.pgemm_split_plan(*args)
 
 
-# ------------------------------------------------ fp32 stream-K head ---------
+# ------------------------------------------------ fp32 stream-K tail ---------
 def sk_slot_ranges(R, T, G):
     total = R * T
     return [(j * total // G, (j + 1) * total // G) for j in range(G)]
