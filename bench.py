@@ -526,7 +526,7 @@ def main():
     ap.add_argument("--hazard", type=int, default=0,
                     help="run the stage-reuse hazard experiment this many iterations per variant")
     ap.add_argument("--point", default=None,
-                    help="dtype,M,N,K,bm,bn,bk,stages[,max_k_parts]: time one point "
+                    help="dtype,M,N,K,bm,bn,bk,stages[,max_k_parts[,producer[,engine]]]: time one point "
                          "(for profiler captures and split / no-split comparisons)")
     args = ap.parse_args()
     if args.warmup < 3:
