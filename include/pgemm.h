@@ -25,9 +25,10 @@
  *     stream): it enqueues work and returns; the caller synchronises.  The
  *     library may enqueue a small repack kernel and stream-ordered scratch
  *     (cudaMallocAsync / cudaFreeAsync) on the same stream when a leading
- *     dimension is not a multiple of 16 bytes, and (bf16, int8) stream-ordered
- *     scratch plus a cudaMemsetAsync of its counters when the last wave of
- *     output tiles is split along K (see pgemm_config.max_k_parts).
+ *     dimension is not a multiple of 16 bytes, and stream-ordered scratch
+ *     for partial sums when tiles are split along K (see
+ *     pgemm_config.max_k_parts), whose counters a cudaMemsetAsync zeroes
+ *     (int8: its widening kernel does).
  *   - M, N, K >= 0.  M == 0 or N == 0: nothing is done.  K == 0: C <- beta*C
  *     (C is not read when beta == 0, so a NaN in C does not survive).
  *   - beta == 0: C is not read (BLAS convention).

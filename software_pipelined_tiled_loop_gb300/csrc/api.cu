@@ -359,9 +359,12 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
             return PGEMM_ERR_CUDA;
         sched.partials = static_cast<uint32_t *>(split_area.p);
         sched.counters = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(split_area.p) + pbytes);
-        // before any pre-pass, so that a programmatic launch after the pre-pass
-        // still finds the counters zero
-        if (cudaMemsetAsync(sched.counters, 0, cbytes, stream) != cudaSuccess) return PGEMM_ERR_CUDA;
+        // The counters start at zero: the int8 widening pass (which the GEMM
+        // waits for) zeroes them; otherwise a memset before any pre-pass does,
+        // so that a programmatic launch after the pre-pass still finds them zero.
+        if (!(KIND == Kind::I8 && k->engine == PGEMM_ENGINE_DEFAULT && K > 0) &&
+            cudaMemsetAsync(sched.counters, 0, cbytes, stream) != cudaSuccess)
+            return PGEMM_ERR_CUDA;
     }
     std::function<cudaError_t()> prepass;  // repack / widening launch, if any
     if (K > 0) {
@@ -402,8 +405,10 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
                 if (widen)  // int8 -> fp16 of both operands in one launch
                     return launch_widen_i8_pair(reinterpret_cast<const int8_t *>(A), lda, base,
                                                 a_ld2, M, K, reinterpret_cast<const int8_t *>(B),
-                                                ldb, base + a_bytes, b_ld2, K, N, d->sm_count,
-                                                stream);
+                                                ldb, base + a_bytes, b_ld2, K, N,
+                                                sched.counters,
+                                                static_cast<int>(sched.counter_words),
+                                                d->sm_count, stream);
                 cudaError_t e = cudaSuccess;
                 if (a_repack)
                     e = launch_repack(A, lda, base, a_ld2, M, K, in_bytes, d->sm_count, stream);

@@ -88,7 +88,12 @@ struct WidenJob {
 constexpr int kWidenRows = 2;
 constexpr int kWidenGroups = 2;
 
-__global__ void __launch_bounds__(256, 6) widen_i8_to_f16_kernel(WidenJob ja, WidenJob jb) {
+__global__ void __launch_bounds__(256, 6) widen_i8_to_f16_kernel(WidenJob ja, WidenJob jb,
+                                                                 uint32_t *zero, int zero_words) {
+    // the GEMM's K-split tickets start at zero (it reads them only after this
+    // grid has completed)
+    if (blockIdx.x == 0 && blockIdx.y == 0)
+        for (int i = threadIdx.x; i < zero_words; i += blockDim.x) zero[i] = 0u;
     const WidenJob &j = blockIdx.y == 0 ? ja : jb;
     if (j.rows <= 0 || j.cols <= 0) return;
     if (j.vec) {
@@ -147,7 +152,8 @@ static WidenJob make_job(const int8_t *src, long long sld, void *dst, long long 
 cudaError_t launch_widen_i8_pair(const int8_t *a, long long lda, void *a_dst, long long a_dld,
                                  int a_rows, int a_cols, const int8_t *b, long long ldb,
                                  void *b_dst, long long b_dld, int b_rows, int b_cols,
-                                 int sm_count, cudaStream_t stream) {
+                                 uint32_t *zero, int zero_words, int sm_count,
+                                 cudaStream_t stream) {
     const WidenJob ja = make_job(a, lda, a_dst, a_dld, a_rows, a_cols);
     const WidenJob jb = make_job(b, ldb, b_dst, b_dld, b_rows, b_cols);
     // vector path: one block per kWidenRows rows; scalar path: about four
@@ -160,7 +166,8 @@ cudaError_t launch_widen_i8_pair(const int8_t *a, long long lda, void *a_dst, lo
     const long long cap = static_cast<long long>(sm_count) * 16;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    widen_i8_to_f16_kernel<<<dim3(static_cast<unsigned>(blocks), 2), 256, 0, stream>>>(ja, jb);
+    widen_i8_to_f16_kernel<<<dim3(static_cast<unsigned>(blocks), 2), 256, 0, stream>>>(ja, jb, zero,
+                                                                                 zero_words);
     return cudaGetLastError();
 }
 

@@ -115,7 +115,8 @@ namespace pg {
 cudaError_t launch_widen_i8_pair(const int8_t *a, long long lda, void *a_dst, long long a_dld,
                                  int a_rows, int a_cols, const int8_t *b, long long ldb,
                                  void *b_dst, long long b_dld, int b_rows, int b_cols,
-                                 int sm_count, cudaStream_t stream);
+                                 uint32_t *zero, int zero_words, int sm_count,
+                                 cudaStream_t stream);
 }  // namespace pg
 
 namespace pg {
