@@ -105,18 +105,16 @@ typedef enum { PGEMM_ENGINE_DEFAULT = 0, PGEMM_ENGINE_MMA_SYNC = 1 } pgemm_engin
  * pipelines and asynchronous copies", section "Selecting the number of
  * stages").  Zero fields mean "library default for this shape".
  *
- * max_k_parts (bf16 and int8; the pages have no counterpart): the tensor-core
- * kernels are persistent, one work unit per resident CTA (or CTA pair) at a
- * time.  When the output tiles would leave the last wave at most half full,
- * as many tiles as that wave would hold are cut along K into P parts each
- * (P <= resident units / those tiles, P <= 8, every part at least 1024 of K)
- * and run first, side by side; the last part of a tile to finish adds the
- * others' partial sums (fp32, in part order, so the result does not depend
- * on timing; int8: exact int32) before the alpha/beta update.  max_k_parts =
- * 0: that choice; 1: never split; n > 1: at most n parts.  fp32 (TMA
- * producer) is persistent too and deals the leftover tiles' K-iterations out
- * to every resident block instead (pgemm_stream_k_plan); max_k_parts = 1
- * turns that off, other values leave it on. */
+ * max_k_parts (the pages have no counterpart): stream-K against wave
+ * quantisation (pgemm_stream_k_plan).  The tiles a partial last wave would
+ * hold have their K-iterations dealt out to every resident CTA (or CTA pair);
+ * the persistent tensor-core kernels run a slot's pieces before its whole
+ * tiles, fp32 runs them as a second grid behind the whole tiles.  The last
+ * piece of a tile to finish adds the others' partial sums (fp32 sums in slot
+ * order, so the result does not depend on timing; int8: exact int32) before
+ * the alpha/beta update.  max_k_parts = 0: the library's choice (at most 2
+ * pieces a tile for the tensor-core kernels, whose exchange is slower than
+ * the fp32 kernels'; none for fp32); 1: off; n > 1: at most n pieces a tile. */
 typedef struct {
     int bm, bn, bk, stages;
     int max_k_parts;
@@ -210,34 +208,25 @@ PGEMM_API pgemm_status pgemm_schedule(pgemm_dtype dtype, const pgemm_config *cfg
                                       int K, long long *tiles, int *slots,
                                       long long *split_tiles, int *parts);
 
-/* The K-split rule itself, a pure host computation (no device needed): for
- * `tiles` output tiles on `slots` schedule slots, K of `k_tiles` K-tiles and
- * accumulation rounds of `round_tiles` K-tiles (0: one round per tile), with
- * the cap `max_parts` (as in pgemm_config).  Outputs: how many tiles are
- * split (0 when none; they are the first tiles of the schedule and run
- * first), the parts per split tile (1 when none), the granule in K-tiles that
- * parts are made of, and the number of whole granules in K.  Part j of a
- * split tile covers granules [j * granules / parts, (j + 1) * granules /
- * parts); the last part also the K-tiles beyond `granules` whole granules. */
-PGEMM_API pgemm_status pgemm_split_plan(long long tiles, int slots, int k_tiles, int round_tiles,
-                                        int max_parts, long long *split_tiles, int *parts,
-                                        int *gran, int *granules);
-
-/* The stream-K rule of the persistent fp32 kernels, a pure host computation
- * (no device needed; the pages have no counterpart).  `tiles` output tiles on
- * `slots` resident blocks with K of `k_tiles` K-tiles: when tiles % slots = R
- * > 0, the R * k_tiles K-iterations of R tiles give every slot at least 8 and
- * the longest share is at most 7/8 of k_tiles, those K-iterations are dealt
- * out first, slot j taking iterations
- * [j * R * k_tiles / slots, (j + 1) * R * k_tiles / slots) of the R tiles laid
- * end to end; then each slot takes whole tiles R + j, R + j + slots, ...
- * Outputs: R (0 when nothing is dealt out), the most slots any such tile is
- * spread over (1 when none), and the K-iterations per slot.  The pieces of a
- * tile each store their partial sums; the last to finish adds them in slot
- * order (so results do not depend on timing) and writes C.  max_parts = 1
- * turns it off (as pgemm_config.max_k_parts = 1 does for a call). */
+/* The stream-K rule, a pure host computation (no device needed; the pages
+ * have no counterpart).  `tiles` output tiles on `slots` schedule slots
+ * (resident blocks, or CTA pairs) with K of `k_tiles` K-tiles: the
+ * R = tiles % slots tiles of the partial last wave have their R * k_tiles
+ * K-iterations laid end to end and dealt out to Gs slots, slot j taking
+ * [j * R * k_tiles / Gs, (j + 1) * R * k_tiles / Gs) -- pieces of at most
+ * two tiles -- and every slot then takes whole tiles R + j, R + j + slots, ...
+ * Gs = slots, unless max_parts = n > 1 and some tile would be spread over
+ * more than n slots: then Gs = R * p with p = min(n, slots / R), and every
+ * tile is exactly p pieces.  Used only when every slot gets at least 8
+ * K-iterations and the longest share is at most 7/8 of k_tiles; max_parts = 1
+ * turns it off.  The pieces of a tile each leave their partial sums; one adds
+ * them in slot order (so results do not depend on timing) and writes C.
+ * Outputs: R (0 when unused), Gs, the most slots one tile is spread over (1
+ * when unused) and the K-iterations per slot.  The library calls it with
+ * pgemm_config.max_k_parts, or with 2 (tensor-core kernels) and 0 (fp32) when
+ * that is 0. */
 PGEMM_API pgemm_status pgemm_stream_k_plan(long long tiles, int slots, int k_tiles, int max_parts,
-                                           long long *sk_tiles, int *max_pieces,
+                                           long long *sk_tiles, int *sk_slots, int *max_pieces,
                                            long long *share);
 
 /* The stage-reuse hazard experiment of "Software pipelines and asynchronous

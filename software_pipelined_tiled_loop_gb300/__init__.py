@@ -20,7 +20,7 @@ __all__ = [
     "gemm_bf16_ex", "gemm_i8_ex", "pgemm_default_config", "pgemm_list_configs",
     "pgemm_kernel_attrs", "pgemm_get_device_status", "pgemm_selftest_wait_timeout",
     "pgemm_status_string", "pgemm_version", "gemm_i8_noalloc", "NOALLOC_SCRATCH_BYTES",
-    "pgemm_stage_reuse_demo", "pgemm_schedule", "pgemm_split_plan", "pgemm_stream_k_plan",
+    "pgemm_stage_reuse_demo", "pgemm_schedule", "pgemm_stream_k_plan",
     "DTYPES", "STATUS", "EXPORTED", "PRODUCERS", "ENGINES",
 ]
 
@@ -45,7 +45,7 @@ EXPORTED = [
     "pgemm_default_config", "pgemm_list_configs", "pgemm_kernel_attrs",
     "pgemm_get_device_status", "pgemm_selftest_wait_timeout", "pgemm_status_string",
     "pgemm_version", "gemm_i8_noalloc", "pgemm_stage_reuse_demo", "pgemm_schedule",
-    "pgemm_split_plan", "pgemm_stream_k_plan",
+    "pgemm_stream_k_plan",
 ]
 
 
@@ -101,8 +101,7 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
         "pgemm_version": [],
         "pgemm_stage_reuse_demo": [vp, i, i, vp, vp, i, i, ctypes.c_uint, vp, i, vp],
         "pgemm_schedule": [i, cfgp, i, i, i, llp, ip, llp, ip],
-        "pgemm_split_plan": [ll, i, i, i, i, llp, ip, ip, ip],
-        "pgemm_stream_k_plan": [ll, i, i, i, llp, ip, llp],
+        "pgemm_stream_k_plan": [ll, i, i, i, llp, ip, ip, llp],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -231,24 +230,15 @@ def pgemm_schedule(dtype: str, M: int, N: int, K: int, config=None):
     return {"tiles": t.value, "slots": sl.value, "split_tiles": st.value, "parts": p.value}
 
 
-def pgemm_split_plan(tiles: int, slots: int, k_tiles: int, round_tiles: int = 0,
-                     max_parts: int = 0):
-    """The K-split rule (host only): a dict with split_tiles, parts, gran and
-    granules."""
-    sf, p, g, q = ctypes.c_longlong(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
-    _check(lib().pgemm_split_plan(tiles, slots, k_tiles, round_tiles, max_parts,
-                                  ctypes.byref(sf), ctypes.byref(p), ctypes.byref(g),
-                                  ctypes.byref(q)), "pgemm_split_plan")
-    return {"split_tiles": sf.value, "parts": p.value, "gran": g.value, "granules": q.value}
-
-
 def pgemm_stream_k_plan(tiles: int, slots: int, k_tiles: int, max_parts: int = 0):
-    """The stream-K rule of the persistent fp32 kernels (host only): a dict
-    with sk_tiles, max_pieces and share (K-iterations per slot)."""
-    st, mp, sh = ctypes.c_longlong(), ctypes.c_int(), ctypes.c_longlong()
+    """The stream-K rule (host only): a dict with sk_tiles, sk_slots,
+    max_pieces and share (K-iterations per slot)."""
+    st, gs, mp, sh = ctypes.c_longlong(), ctypes.c_int(), ctypes.c_int(), ctypes.c_longlong()
     _check(lib().pgemm_stream_k_plan(tiles, slots, k_tiles, max_parts, ctypes.byref(st),
-                                     ctypes.byref(mp), ctypes.byref(sh)), "pgemm_stream_k_plan")
-    return {"sk_tiles": st.value, "max_pieces": mp.value, "share": sh.value}
+                                     ctypes.byref(gs), ctypes.byref(mp), ctypes.byref(sh)),
+           "pgemm_stream_k_plan")
+    return {"sk_tiles": st.value, "sk_slots": gs.value, "max_pieces": mp.value,
+            "share": sh.value}
 
 
 def pgemm_default_config(dtype: str, M: int, N: int, K: int):

@@ -156,46 +156,38 @@ static pgemm_config default_config(pgemm_dtype dt, int M, int N, int K, int sm_c
     return c;
 }
 
-// Splitting tiles along K against wave quantisation.  A persistent grid of G
-// slots runs `tiles` output tiles in ceil(tiles / G) waves; when the last
-// wave would hold R = tiles % G tiles, at most G / 2, R tiles are instead cut
-// into P = min(G / R, granules of K, 8) parts each, so that the extra wave
-// takes about 1/P of a tile's time instead of a whole one.  The parts run
-// first (the R * P parts fill the first wave, the whole tiles follow), so
-// the exchange of partial sums overlaps whole-tile work in the slots instead
-// of ending the kernel.  A part is at least kSplitGranTiles K-tiles (or one
-// int8 round): below that the exchange costs about what it saves.
-constexpr int kSplitGranTiles = 16;
-constexpr int kMaxSplitParts = 8;
+// Stream-K against wave quantisation.  A persistent grid of G slots runs
+// `tiles` output tiles in ceil(tiles / G) waves; the R = tiles % G tiles of
+// the partial last wave instead have their R * T K-iterations dealt out in
+// equal contiguous ranges to Gs slots (pgemm_stream_k_plan), so that the
+// extra wave costs about R / Gs of a tile.  The persistent tensor-core
+// kernels run these pieces first, each slot's pieces before its whole tiles,
+// so that the exchange of partial sums overlaps whole-tile work; the fp32
+// kernels run them as a second grid behind the whole tiles.  The tensor-core
+// kernels cap a tile at kTcMaxPieces pieces by default (equal halves, on
+// R * 2 slots): their last piece waits for the others' partial sums and adds
+// them in an epilogue warp, one 16 KB slab at a time, and with more pieces
+// that exchange costs more than the shorter shares save (int8 4096^3: 132.5
+// us with up to four pieces, 107.8 with halves, 110.5 without; bf16
+// 2048^2 x 8192, where every slot would share: 65.0 against 57.3 without).
+constexpr int kTcMaxPieces = 2;
 
 static TileSchedule plan_schedule(const KernelInfo &k, int M, int N, int K, int slots,
                                   int max_parts) {
     TileSchedule s;
     s.tiles = static_cast<long long>((M + k.bm - 1) / k.bm) * ((N + k.bn - 1) / k.bn);
     s.slots = slots;
-    s.units = s.tiles;
     if (k.schedule_slots == nullptr) return s;
     const int T = (K + k.bk - 1) / k.bk;
-    if (k.stream_k) {
-        long long share = 0;
-        if (pgemm_stream_k_plan(s.tiles, slots, T, max_parts, &s.split_tiles, &s.parts, &share) !=
-            PGEMM_OK)
-            return s;
-        if (s.split_tiles > 0) {
-            // a slot of partial sums for each of a slot's (at most two) pieces
-            s.partial_words = 2LL * slots * k.bm * k.bn;
-            s.counter_words = s.split_tiles;
-        }
+    const int cap = max_parts > 0 ? max_parts : (k.stream_k ? 0 : kTcMaxPieces);
+    long long share = 0;
+    if (pgemm_stream_k_plan(s.tiles, slots, T, cap, &s.split_tiles, &s.sk_slots, &s.parts,
+                            &share) != PGEMM_OK)
         return s;
-    }
-    if (pgemm_split_plan(s.tiles, slots, T, k.kc, max_parts, &s.split_tiles, &s.parts, &s.gran,
-                         &s.q) != PGEMM_OK)
-        return s;
-    const long long rem = s.split_tiles;
-    s.units = s.tiles + rem * (s.parts - 1);
-    if (s.parts > 1) {
-        s.partial_words = rem * s.parts * k.bm * k.bn;
-        s.counter_words = rem * k.slabs_per_tile * 2;
+    if (s.split_tiles > 0) {
+        // a slab of partial sums for each of a slot's (at most two) pieces
+        s.partial_words = 2LL * s.sk_slots * k.bm * k.bn;
+        s.counter_words = k.stream_k ? s.split_tiles : s.split_tiles * k.slabs_per_tile * 2;
     }
     return s;
 }
@@ -602,62 +594,56 @@ pgemm_status pgemm_kernel_attrs(pgemm_dtype dtype, const pgemm_config *cfg, int 
     return PGEMM_OK;
 }
 
-pgemm_status pgemm_split_plan(long long tiles, int slots, int k_tiles, int round_tiles,
-                              int max_parts, long long *split_tiles, int *parts, int *gran,
-                              int *granules) {
-    if (tiles < 0 || slots < 1 || k_tiles < 0 || round_tiles < 0 || max_parts < 0 ||
-        !split_tiles || !parts || !gran || !granules)
-        return PGEMM_ERR_INVALID_VALUE;
-    *split_tiles = 0;
-    *parts = 1;
-    *gran = round_tiles > 0 ? round_tiles : kSplitGranTiles;
-    *granules = k_tiles / *gran;
-    if (max_parts == 1 || slots < 2 || *granules < 2) return PGEMM_OK;
-    const long long rem = tiles % slots;
-    if (rem == 0) return PGEMM_OK;
-    long long p = slots / rem;
-    if (p > *granules) p = *granules;
-    if (p > kMaxSplitParts) p = kMaxSplitParts;
-    if (max_parts > 1 && p > max_parts) p = max_parts;
-    if (p < 2) return PGEMM_OK;
-    *parts = static_cast<int>(p);
-    *split_tiles = rem;
-    return PGEMM_OK;
-}
-
-// The stream-K head of the persistent FFMA kernels: a piece of a tile is at
-// least kMinStreamKIters K-tiles, below which its exchange would cost about
-// what it saves, and the head is used only when its longest share is at most
-// 7/8 of a tile.
+// A piece of a tile is at least kMinStreamKIters K-tiles, below which its
+// exchange would cost about what it saves; stream-K is used only when the
+// longest share is at most 7/8 of a tile.
 constexpr long long kMinStreamKIters = 8;
 
 pgemm_status pgemm_stream_k_plan(long long tiles, int slots, int k_tiles, int max_parts,
-                                 long long *sk_tiles, int *max_pieces, long long *share) {
-    if (tiles < 0 || slots < 1 || k_tiles < 0 || max_parts < 0 || !sk_tiles || !max_pieces ||
-        !share)
+                                 long long *sk_tiles, int *sk_slots, int *max_pieces,
+                                 long long *share) {
+    if (tiles < 0 || slots < 1 || k_tiles < 0 || max_parts < 0 || !sk_tiles || !sk_slots ||
+        !max_pieces || !share)
         return PGEMM_ERR_INVALID_VALUE;
     *sk_tiles = 0;
+    *sk_slots = 0;
     *max_pieces = 1;
     *share = 0;
     if (max_parts == 1 || k_tiles == 0 || slots < 2) return PGEMM_OK;
     const long long rem = tiles % slots;
     if (rem == 0) return PGEMM_OK;
     const long long total = rem * k_tiles;
-    if (total / slots < kMinStreamKIters) return PGEMM_OK;
+    // the most slots one of the R tiles is spread over, with g slots taking part
+    auto most_pieces = [&](long long g) {
+        // slot holding iteration x: the largest j with j * total / g <= x
+        auto slot_of = [&](long long x) { return ((x + 1) * g - 1) / total; };
+        long long most = 1;
+        for (long long r = 0; r < rem; ++r) {
+            const long long p = slot_of((r + 1) * k_tiles - 1) - slot_of(r * k_tiles) + 1;
+            if (p > most) most = p;
+        }
+        return most;
+    };
+    long long g = slots;
+    long long most = most_pieces(g);
+    if (max_parts > 1 && most > max_parts) {
+        // capped: g = R * p slots, p = min(cap, G / R), so that every tile is
+        // exactly p pieces (slot r * p starts tile r)
+        long long p = slots / rem;
+        if (p > max_parts) p = max_parts;
+        if (p < 2) return PGEMM_OK;
+        g = rem * p;
+        most = p;
+    }
+    if (total / g < kMinStreamKIters) return PGEMM_OK;
     // worth it only if the longest share saves at least an eighth of a tile
     // over the extra wave it replaces
-    const long long longest = (total + slots - 1) / slots;
+    const long long longest = (total + g - 1) / g;
     if (longest * 8 > static_cast<long long>(k_tiles) * 7) return PGEMM_OK;
-    // slot holding stream-K iteration x: the largest j with j * total / slots <= x
-    auto slot_of = [&](long long x) { return ((x + 1) * slots - 1) / total; };
-    long long most = 1;
-    for (long long r = 0; r < rem; ++r) {
-        const long long p = slot_of((r + 1) * k_tiles - 1) - slot_of(r * k_tiles) + 1;
-        if (p > most) most = p;
-    }
     *sk_tiles = rem;
+    *sk_slots = static_cast<int>(g);
     *max_pieces = static_cast<int>(most);
-    *share = total / slots;
+    *share = total / g;
     return PGEMM_OK;
 }
 

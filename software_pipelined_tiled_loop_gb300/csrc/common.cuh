@@ -32,16 +32,15 @@ struct GemmArgs {
     Out *C;           // row-major, leading dimension ldc
     long long ldc;
     int c_tma;        // 1: C is also described by a tensor map (TMA stores allowed)
-    // Work units of the persistent tensor-core kernels, strided over the grid.
-    // The first split_tiles output tiles are each cut along K into
-    // split_parts parts and come first: unit i * split_parts + j is part j of
-    // tile i and covers granules [j * split_q / split_parts, (j + 1) *
-    // split_q / split_parts) of split_gran K-tiles each, the last part also
-    // the K-tiles beyond split_q granules.  Then every other tile is one
-    // unit.  The parts of a tile meet through `partials` (raw partial sums)
-    // and `counters` (two per epilogue slab, zero at launch).  No split:
-    // split_tiles = 0, split_parts = 1.
-    int num_units, split_tiles, split_parts, split_gran, split_q;
+    // Stream-K schedule of the persistent kernels: the K-iterations of the
+    // first split_tiles output tiles (R tiles, R * T iterations laid end to
+    // end) are dealt out to slots 0 .. sk_slots - 1, slot j taking
+    // [j * R * T / sk_slots, (j + 1) * R * T / sk_slots): pieces of at most
+    // two tiles.  The other tiles are whole units, tile R + j + i * G for
+    // slot j of G.  The pieces of a tile meet through `partials` (raw partial
+    // sums, one slab per slot and piece) and `counters` (zero at launch).
+    // None: split_tiles = 0.
+    int split_tiles, sk_slots;
     uint32_t *partials;
     uint32_t *counters;
 };

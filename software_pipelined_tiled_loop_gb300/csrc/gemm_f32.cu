@@ -722,7 +722,7 @@ static cudaError_t launch_f32_impl(const LaunchF32 &p, cudaStream_t stream) {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t lc{};
-    lc.gridDim = dim3(static_cast<unsigned>(p.sched.slots));
+    lc.gridDim = dim3(static_cast<unsigned>(p.sched.sk_slots));
     lc.blockDim = dim3(Cfg::THREADS);
     lc.dynamicSmemBytes = Cfg::SMEM_BYTES;
     lc.stream = stream;

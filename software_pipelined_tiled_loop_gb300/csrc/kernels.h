@@ -22,20 +22,18 @@ constexpr int smem_request(int used, int max_blocks) {
     return used > cap ? used : cap;
 }
 
-// How a call's output tiles are spread over a persistent tensor-core grid:
-// `slots` units run at once (resident CTAs, or CTA pairs); when the tiles
-// would leave the last wave at most half full, that many tiles
-// (`split_tiles`) are each cut along K into `parts` parts (whole granules of
-// `gran` K-tiles, `q` granules covering K) and scheduled first.
-// partials / counters: the split tiles' meeting area (counters zeroed before
-// the launch).
+// How a call's output tiles are spread over a persistent grid: `slots`
+// units run at once (resident blocks, or CTA pairs); the `split_tiles`
+// leftover tiles of a partial last wave have their K-iterations dealt out to
+// `sk_slots` slots (stream-K), at most `parts` slots sharing one tile.
+// partials / counters: the meeting area of those pieces (counters zeroed
+// before the launch).
 struct TileSchedule {
     long long tiles = 0;
     int slots = 0;
     long long split_tiles = 0;
+    int sk_slots = 0;
     int parts = 1;
-    int gran = 1, q = 0;
-    long long units = 0;
     long long partial_words = 0, counter_words = 0;
     uint32_t *partials = nullptr;
     uint32_t *counters = nullptr;

@@ -28,12 +28,13 @@
 // products of int8 values stay integers of magnitude <= 2^24 and are exact;
 // the epilogue converts each chunk to int32 and adds it into registers).
 //
-// The kernel is persistent (grid = resident blocks, work units strided by
-// the grid; the pipeline prologue is paid once per block, not once per tile)
-// and TMEM holds two accumulators, so the epilogue of one round overlaps the
-// main loop of the next.  A work unit is an output tile, or one K part of a
-// tile split against wave quantisation (GemmArgs); the parts of a split tile
-// run first and meet through global memory (SplitSlab).  Stage index t % S
+// The kernel is persistent (grid = resident blocks, each walking its own list
+// of work units; the pipeline prologue is paid once per block, not once per
+// tile) and TMEM holds two accumulators, so the epilogue of one round
+// overlaps the main loop of the next.  A work unit is an output tile, or a
+// stream-K piece of one of the tiles a partial last wave would leave over
+// (GemmArgs, SlotPlan); a slot's pieces run first and meet the other pieces
+// of their tiles through global memory (SplitSlab).  Stage index t % S
 // and phase parity (t / S) & 1 come from a running counter, valid for any S
 // (the page's XOR swap is valid for two stages only).
 //
@@ -181,32 +182,72 @@ __device__ __forceinline__ void release_acc(uint64_t *acc_empty_bar) {
 }
 
 // One work unit of the persistent schedule: an output tile (schedule index)
-// and the K-tiles [kb, ke) it accumulates; part >= 0 for a part of a tile
-// split along K (`split` numbers the split tiles from 0).
+// and the K-tiles [kb, ke) it accumulates.  For a stream-K piece, part >= 0
+// is its place among the `parts` slots sharing the tile, slab numbers its
+// partial-sum slab (two per slot: slot * 2 + the piece's place in the slot's
+// list) and slab0 the slab of the tile's piece 0.  Pieces 1, 2, ... start
+// inside the tile, so each is its slot's first piece: slab (first slot + j)
+// * 2; piece 0 is its slot's second piece when that slot began in the tile
+// before.
 struct WorkUnit {
-    int tile, kb, ke, part, split;
+    int tile, kb, ke, part, parts, slab, slab0;
 };
 
-template <typename A>
-__device__ __forceinline__ WorkUnit work_unit(int u, const A &a) {
-    WorkUnit w;
-    const int split_units = a.split_tiles * a.split_parts;
-    if (u >= split_units) {
-        w.tile = u - split_units + a.split_tiles;
+// A slot's list of work units (GemmArgs: the stream-K schedule): first its
+// stream-K pieces (at most two), then its whole tiles.  Producer, MMA issuer
+// and epilogue walk the same list.  Held in shared memory and written once,
+// with the pieces decoded in full there, so that walking the list costs no
+// 64-bit divisions (and no registers) in the loops.
+struct SlotPlan {
+    int T, R, G, j;
+    int n_sk, n_whole;
+    WorkUnit piece[2];
+
+    template <typename A>
+    __device__ __forceinline__ void init(const A &a, int slot, int slots, int tiles) {
+        T = a.num_k_tiles;
+        R = a.split_tiles;
+        G = slots;
+        j = slot;
+        const int Gs = a.sk_slots;
+        const long long total = static_cast<long long>(R) * T;
+        const bool in_sk = R > 0 && slot < Gs;
+        const long long sk_a = in_sk ? slot * total / Gs : 0;
+        const long long sk_end = in_sk ? (slot + 1) * total / Gs : 0;
+        n_sk = sk_end == sk_a ? 0 : ((sk_a / T) == ((sk_end - 1) / T) ? 1 : 2);
+        // the slot holding stream-K iteration x
+        auto slot_of = [&](long long x) { return static_cast<int>(((x + 1) * Gs - 1) / total); };
+        for (int u = 0; u < n_sk; ++u) {
+            WorkUnit &w = piece[u];
+            w.tile = static_cast<int>(sk_a / T) + u;
+            const long long t0 = static_cast<long long>(w.tile) * T;
+            const long long lo = sk_a > t0 ? sk_a : t0;
+            const long long hi = sk_end < t0 + T ? sk_end : t0 + T;
+            w.kb = static_cast<int>(lo - t0);
+            w.ke = static_cast<int>(hi - t0);
+            const int first = slot_of(t0), last = slot_of(t0 + T - 1);
+            w.part = slot - first;
+            w.parts = last - first + 1;
+            w.slab = slot * 2 + u;
+            w.slab0 = first * 2 + (first * total / Gs < t0 ? 1 : 0);
+        }
+        const int whole = tiles - R;
+        n_whole = slot < whole ? (whole - slot + slots - 1) / slots : 0;
+    }
+    __device__ __forceinline__ int units() const { return n_sk + n_whole; }
+    __device__ __forceinline__ WorkUnit unit(int u) const {
+        if (u < n_sk) return piece[u];
+        WorkUnit w;
+        w.tile = R + j + (u - n_sk) * G;
         w.kb = 0;
-        w.ke = a.num_k_tiles;
+        w.ke = T;
         w.part = -1;
-        w.split = 0;
+        w.parts = 1;
+        w.slab = 0;
+        w.slab0 = 0;
         return w;
     }
-    w.split = u / a.split_parts;
-    w.part = u - w.split * a.split_parts;
-    w.tile = w.split;
-    w.kb = w.part * a.split_q / a.split_parts * a.split_gran;
-    w.ke = w.part == a.split_parts - 1 ? a.num_k_tiles
-                                       : (w.part + 1) * a.split_q / a.split_parts * a.split_gran;
-    return w;
-}
+};
 
 // Accumulation rounds of a unit: chunks of KC K-tiles, or all of its K range.
 template <class Cfg>
@@ -219,73 +260,90 @@ __device__ __forceinline__ int unit_rounds(const WorkUnit &w) {
     return w.ke > w.kb ? (w.ke - w.kb + kct - 1) / kct : 0;
 }
 
-// Where the parts of a K-split tile meet, for one epilogue warp's slab of
-// 32 rows x EPI_COLS columns: one slot of raw partial sums per part and two
-// counters (parts arrived, partials written).  A warp arrives once its own
-// sums are in registers.  Every part but the last to arrive stores its
-// partial into its slot and then counts it written (release); the last one
-// waits until all the others are written (acquire) and adds them, in part
-// order, to its own before the alpha/beta update.  The parts it waits for
-// have arrived, so they are past every wait of their own: the exchange cannot
-// deadlock whatever part of the grid is resident, and nobody waits on a part
-// that has not started.
+// Where the stream-K pieces of a tile meet, for one epilogue warp's part of
+// the tile (32 rows x EPI_COLS columns): a slab of raw partial sums per
+// piece (two slabs per slot, one for each of its pieces) and two counters per
+// tile and warp (pieces arrived, partials written).  A warp arrives once its
+// own sums are in registers.  Every piece but the last to arrive stores its
+// partial into its slab and then counts it written (release); the last one
+// waits until all the others are written (acquire) and adds them, in piece
+// order (slot order), to its own before the alpha/beta update.  The pieces it
+// waits for have arrived, so they are past every wait of their own: the
+// exchange cannot deadlock whatever part of the grid is resident, and nobody
+// waits on a piece that has not started.
 //
-// Slot layout: 16-byte group g (columns 4g .. 4g+3) of row r at word
+// Slab layout: 16-byte group g (columns 4g .. 4g+3) of row r at word
 // (g * 32 + r) * 4, so that each store or load of a warp covers 512
 // consecutive bytes.
 template <class Cfg>
 struct SplitSlab {
-    static constexpr int kSlotWords = 32 * Cfg::EPI_COLS;
-    uint32_t *slots;      // part 0's slot; part j's at slots + j * kSlotWords
-    uint32_t *counters;   // [0] parts arrived, [1] partials written
-    int parts, part;
+    static constexpr int kSlabWords = 32 * Cfg::EPI_COLS;
+    // Few registers: the int8 epilogue holds 128 sums beside this.  Pointers
+    // are re-derived from the kernel arguments (WorkUnit: the slab numbers).
+    int tile, part, parts, own, sub, slab0;  // sub: crank * EPI + e, this warp's share
     bool last;
 
-    __device__ __forceinline__ SplitSlab() : slots(nullptr), counters(nullptr), parts(1), part(0), last(true) {}
+    __device__ __forceinline__ SplitSlab()
+        : tile(0), part(0), parts(1), own(0), sub(0), slab0(0), last(true) {}
 
     template <typename A>
-    __device__ __forceinline__ SplitSlab(const A &a, const WorkUnit &w, uint32_t crank, uint32_t e) {
-        const long long slab = (static_cast<long long>(w.split) * Cfg::CM + crank) * Cfg::EPI + e;
-        parts = a.split_parts;
-        part = w.part;
-        slots = a.partials + slab * parts * kSlotWords;
-        counters = a.counters + 2 * slab;
+    __device__ __forceinline__ SplitSlab(const A &a, const SlotPlan &sp, const WorkUnit &w,
+                                         uint32_t crank, uint32_t e)
+        : tile(w.tile), part(w.part), parts(w.parts), own(w.slab),
+          sub(static_cast<int>(crank) * Cfg::EPI + static_cast<int>(e)), slab0(w.slab0) {
         uint32_t old = 0;
-        if (lane_id() == 0) old = atomicAdd(counters, 1u);
+        if (lane_id() == 0) old = atomicAdd(counters(a), 1u);
         old = __shfl_sync(0xffffffffu, old, 0);
         last = old == static_cast<uint32_t>(parts - 1);
     }
 
-    // The last part: wait until every other part's partial is written.
-    __device__ __forceinline__ bool wait_others(const KernelCtx &ctx) const {
+    // [0] pieces arrived, [1] partials written
+    template <typename A>
+    __device__ __forceinline__ uint32_t *counters(const A &a) const {
+        return a.counters + 2 * (static_cast<long long>(tile) * Cfg::CM * Cfg::EPI + sub);
+    }
+    template <typename A>
+    __device__ __forceinline__ uint32_t *slab(const A &a, int s) const {
+        return a.partials + (static_cast<long long>(s) * Cfg::CM * Cfg::EPI + sub) * kSlabWords;
+    }
+
+    // The last piece: wait until every other piece's partial is written.
+    template <typename A>
+    __device__ __forceinline__ bool wait_others(const A &a, const KernelCtx &ctx) const {
         bool ok = true;
         if (lane_id() == 0)
-            ok = wait_counter(counters + 1, static_cast<uint32_t>(parts - 1), ctx, kSiteSplitPartial);
+            ok = wait_counter(counters(a) + 1, static_cast<uint32_t>(parts - 1), ctx,
+                              kSiteSplitPartial);
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         __syncwarp();
         __threadfence();
         return ok;
     }
 
-    // Store 32 columns [c, c + 32) of this lane's row as this part's partial.
-    __device__ __forceinline__ void put(int c, const uint32_t *v) const {
-        uint4 *dst = reinterpret_cast<uint4 *>(slots + part * kSlotWords) + (c / 4) * 32 + lane_id();
+    // Store 32 columns [c, c + 32) of this lane's row as this piece's partial.
+    template <typename A>
+    __device__ __forceinline__ void put(const A &a, int c, const uint32_t *v) const {
+        uint4 *dst = reinterpret_cast<uint4 *>(slab(a, own)) + (c / 4) * 32 + lane_id();
 #pragma unroll
         for (int g = 0; g < 8; ++g)
             dst[g * 32] = make_uint4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
     }
 
     // After the last put: count this partial as written.
-    __device__ __forceinline__ void publish() const {
+    template <typename A>
+    __device__ __forceinline__ void publish(const A &a) const {
         __threadfence();
         __syncwarp();
-        if (lane_id() == 0) red_release_add(counters + 1, 1u);
+        if (lane_id() == 0) red_release_add(counters(a) + 1, 1u);
     }
 
-    // Part j's 32 columns [c, c + 32) of this lane's row (j != part).
-    __device__ __forceinline__ void get(int j, int c, uint32_t *v) const {
-        const uint4 *src =
-            reinterpret_cast<const uint4 *>(slots + j * kSlotWords) + (c / 4) * 32 + lane_id();
+    // Piece j's 32 columns [c, c + 32) of this lane's row (j != part): the
+    // piece of slot (this slot - part + j).
+    template <typename A>
+    __device__ __forceinline__ void get(const A &a, const SlotPlan &sp, int j, int c,
+                                        uint32_t *v) const {
+        const int s = j == 0 ? slab0 : (sp.j - part + j) * 2;
+        const uint4 *src = reinterpret_cast<const uint4 *>(slab(a, s)) + (c / 4) * 32 + lane_id();
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
             const uint4 x = __ldcg(src + g * 32);
@@ -296,14 +354,16 @@ struct SplitSlab {
         }
     }
 
-    // v <- the sum over all parts of columns [c, c + 32), v holding this
-    // part's own values on entry.  fp32: added in part order, P0 + P1 + ...,
-    // whichever part arrived last, so the result does not depend on timing.
-    __device__ __forceinline__ void reduce_f32(int c, uint32_t *v) const {
+    // v <- the sum over all pieces of columns [c, c + 32), v holding this
+    // piece's own values on entry.  fp32: added in piece order, P0 + P1 + ...,
+    // whichever piece arrived last, so the result does not depend on timing.
+    template <typename A>
+    __device__ __forceinline__ void reduce_f32(const A &a, const SlotPlan &sp, int c,
+                                               uint32_t *v) const {
         float sum[32];
         uint32_t t[32];
         for (int j = 0; j < parts; ++j) {
-            if (j != part) get(j, c, t);
+            if (j != part) get(a, sp, j, c, t);
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 const float x = __uint_as_float(j == part ? v[i] : t[i]);
@@ -314,12 +374,14 @@ struct SplitSlab {
         for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(sum[i]);
     }
 
-    // int32: v += every other part's values, modulo 2^32 (order-free).
-    __device__ __forceinline__ void reduce_i32(int c, uint32_t *v) const {
+    // int32: v += every other piece's values, modulo 2^32 (order-free).
+    template <typename A>
+    __device__ __forceinline__ void reduce_i32(const A &a, const SlotPlan &sp, int c,
+                                               uint32_t *v) const {
         uint32_t t[32];
         for (int j = 0; j < parts; ++j) {
             if (j == part) continue;
-            get(j, c, t);
+            get(a, sp, j, c, t);
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] += t[i];
         }
@@ -346,11 +408,17 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     uint64_t *acc_empty = acc_full + 2;   // [2]
     uint64_t *mma_done = acc_empty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+    __shared__ SlotPlan sp;  // this slot's list of work units
 
     const uint32_t warp = warp_id_uniform();
     const uint32_t lane = lane_id();
+    // Cluster geometry: with a CTA pair a "tile" of the schedule is a 2 x 1
+    // stack of 128-row tiles; this CTA computes the one at its cluster rank.
+    const int num_m_sched = (args.num_m_tiles + Cfg::CM - 1) / Cfg::CM;
 
     if (warp == 0 && lane == 0) {
+        sp.init(args, static_cast<int>(blockIdx.x) / Cfg::CM, static_cast<int>(gridDim.x) / Cfg::CM,
+                num_m_sched * args.num_n_tiles);
         prefetch_tmap(&tmap_a);
         prefetch_tmap(&tmap_b);
         if (args.c_tma) prefetch_tmap(&tmap_c);
@@ -389,21 +457,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     // being written by a pre-pass launched just before (widening, repack).
     grid_dependency_wait();
 
-    // Cluster geometry: with a CTA pair a "tile" of the schedule is a 2 x 1
-    // stack of 128-row tiles; this CTA computes the one at its cluster rank.
     const uint32_t crank = Cfg::CM > 1 ? cluster_ctarank() : 0u;
-    const int sched_id = static_cast<int>(blockIdx.x) / Cfg::CM;
-    const int sched_stride = static_cast<int>(gridDim.x) / Cfg::CM;
-    const int num_m_sched = (args.num_m_tiles + Cfg::CM - 1) / Cfg::CM;
-    const int num_units = args.num_units;
+    const int num_units = sp.units();
 
     if (warp == 0) {
         if (lane == 0) {
             // ---------------- producer: TMA into the stage ring ----------------
             uint32_t it = 0;
             bool ok = true;
-            for (int u = sched_id; ok && u < num_units; u += sched_stride) {
-                const WorkUnit w = work_unit(u, args);
+            for (int u = 0; ok && u < num_units; ++u) {
+                const WorkUnit w = sp.unit(u);
                 int m0, n0;
                 tile_origin(w.tile, num_m_sched, args.num_n_tiles, args.group_m, BM * Cfg::CM, BN, m0,
                             n0);
@@ -456,8 +519,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             constexpr uint16_t kPair = 3;  // both CTAs of the pair
             uint32_t it = 0, gr = 0;
             bool ok = true;
-            for (int u = sched_id; ok && u < num_units; u += sched_stride) {
-                const WorkUnit w = work_unit(u, args);
+            for (int u = 0; ok && u < num_units; ++u) {
+                const WorkUnit w = sp.unit(u);
                 const int kct = unit_round_tiles<Cfg>(w);
                 const int rounds = unit_rounds<Cfg>(w);
                 for (int r = 0; ok && r < rounds; ++r, ++gr) {
@@ -524,18 +587,20 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         const bool tma_path = args.c_tma && args.beta == Scalar(0);
         uint32_t gr = 0;
         bool ok = true;
-        for (int u = sched_id; ok && u < num_units; u += sched_stride) {
-            const WorkUnit w = work_unit(u, args);
-            const int rounds = unit_rounds<Cfg>(w);
-            int m0, n0;
+        // The unit's place in C: rows [m_base, m_base + 32) of this warp's
+        // quadrant, columns from n0 (rows below C take no part, and a
+        // stream-K piece there exchanges nothing: the same for every piece).
+        auto place = [&](const WorkUnit &w, int &m_base, int &n0, bool &in_range, bool &split) {
+            int m0;
             tile_origin(w.tile, num_m_sched, args.num_n_tiles, args.group_m, BM * Cfg::CM, BN, m0, n0);
             m0 += static_cast<int>(crank) * BM;
-            const bool in_range = m0 < args.M;  // the second tile of a pair may lie below C
-            const int m_base = m0 + static_cast<int>(q * 32);
-            // A part of a K-split tile exchanges partial sums (rows below C,
-            // the same for every part, take no part in it).
-            const bool split = w.part >= 0 && in_range;
+            in_range = m0 < args.M;  // the second tile of a pair may lie below C
+            m_base = m0 + static_cast<int>(q * 32);
+            split = w.part >= 0 && in_range;
+        };
+        for (int u = 0; ok && u < num_units; ++u) {
             if constexpr (Cfg::INT_FOLD) {
+                const int rounds = unit_rounds<Cfg>(sp.unit(u));
                 // Exact int8: sum the rounds' integer-valued fp32 partials in
                 // int32.  Rounds of at most 256 products (|x| <= 2^22) convert
                 // with one FADD: for an integer-valued x with |x| <= 2^22,
@@ -580,17 +645,23 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     kMagicFold ? static_cast<uint32_t>(rounds) * 0x4B400000u : 0u;  // mod 2^32
 #pragma unroll
                 for (int j = 0; j < Cfg::EPI_COLS; ++j) acc[j] -= bias;
+                // the unit again, from the shared plan: nothing of it stays in
+                // registers while the 128 sums are built
+                const WorkUnit w = sp.unit(u);
+                int m_base, n0;
+                bool in_range, split;
+                place(w, m_base, n0, in_range, split);
                 if (split) {
-                    const SplitSlab<Cfg> slab(args, w, crank, e);
+                    const SplitSlab<Cfg> slab(args, sp, w, crank, e);
                     if (!slab.last) {
 #pragma unroll
-                        for (int c = 0; c < Cfg::EPI_COLS; c += 32) slab.put(c, acc + c);
-                        slab.publish();
+                        for (int c = 0; c < Cfg::EPI_COLS; c += 32) slab.put(args, c, acc + c);
+                        slab.publish(args);
                         continue;
                     }
-                    if (!slab.wait_others(ctx)) break;
+                    if (!slab.wait_others(args, ctx)) break;
 #pragma unroll
-                    for (int c = 0; c < Cfg::EPI_COLS; c += 32) slab.reduce_i32(c, acc + c);
+                    for (int c = 0; c < Cfg::EPI_COLS; c += 32) slab.reduce_i32(args, sp, c, acc + c);
                 }
                 if (in_range) {
 #pragma unroll
@@ -599,6 +670,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                                       rounds > 0, tma_path);
                 }
             } else {
+                const WorkUnit w = sp.unit(u);
+                const int rounds = unit_rounds<Cfg>(w);
+                int m_base, n0;
+                bool in_range, split;
+                place(w, m_base, n0, in_range, split);
                 if (rounds > 0) {
                     const uint32_t ab = gr & 1u, aph = (gr >> 1) & 1u;
                     if (!mbar_wait(&acc_full[ab], aph, ctx, kSiteEpilogueFull)) break;
@@ -607,10 +683,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         tmem_base + ((q * 32u) << 16) + ab * Cfg::ACC_COLS + col0;
                     // role in a K-split tile: store a partial, or add them all
                     int role = 0;  // 0: whole tile, 1: store partial, 2: reduce
-                    SplitSlab<Cfg> slab = split ? SplitSlab<Cfg>(args, w, crank, e) : SplitSlab<Cfg>();
+                    SplitSlab<Cfg> slab = split ? SplitSlab<Cfg>(args, sp, w, crank, e) : SplitSlab<Cfg>();
                     if (split) {
                         role = slab.last ? 2 : 1;
-                        if (role == 2 && !slab.wait_others(ctx)) ok = false;
+                        if (role == 2 && !slab.wait_others(args, ctx)) ok = false;
                     }
 #pragma unroll 1
                     for (int c = 0; c < Cfg::EPI_COLS; c += 32) {
@@ -625,15 +701,15 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         }
                         if (!ok) continue;
                         if (role == 1) {
-                            slab.put(c, v);
+                            slab.put(args, c, v);
                             continue;
                         }
-                        if (role == 2) slab.reduce_f32(c, v);
+                        if (role == 2) slab.reduce_f32(args, sp, c, v);
                         if (in_range)
                             store_block32<Cfg::STAGE_BUFS>(args, &tmap_c, next_buf(), m_base, n0 + col0 + c, v, true,
                                           tma_path);
                     }
-                    if (role == 1) slab.publish();
+                    if (role == 1) slab.publish(args);
                     ++gr;
                 } else {
                     // K == 0: C = beta * C, tensor memory is never read
@@ -685,11 +761,8 @@ static cudaError_t launch_tc(const P &p, cudaStream_t stream) {
     a.ldc = p.ldc;
     a.c_tma = p.tmap_c != nullptr ? 1 : 0;
     const TileSchedule &sc = p.sched;
-    a.num_units = static_cast<int>(sc.units);
     a.split_tiles = static_cast<int>(sc.split_tiles);
-    a.split_parts = sc.parts;
-    a.split_gran = sc.gran;
-    a.split_q = sc.q;
+    a.sk_slots = sc.sk_slots;
     a.partials = sc.partials;
     a.counters = sc.counters;
     const CUtensorMap &tc = p.tmap_c != nullptr ? *p.tmap_c : *p.tmap_a;
@@ -709,7 +782,9 @@ static cudaError_t launch_tc(const P &p, cudaStream_t stream) {
     lc.stream = stream;
     lc.attrs = attr;
     // one CTA (or CTA pair) per schedule slot, at most one per work unit
-    const long long units = sc.units;
+    // every slot when pieces are dealt out (the plan is made for sc.slots),
+    // else at most one slot per tile
+    const long long units = sc.split_tiles > 0 ? sc.slots : sc.tiles;
     const int grid_units = static_cast<int>(units < sc.slots ? units : sc.slots);
     if (grid_units < 1) return cudaSuccess;
     lc.gridDim = dim3(Cfg::CM * grid_units);

@@ -1,14 +1,14 @@
-"""Parity of the K-split last wave of the persistent tensor-core kernels.
+"""Parity of the stream-K schedule of the persistent tensor-core kernels.
 
-When the output tiles leave the last wave of the persistent grid at most half
-full, each tile of that wave is cut along K into parts whose partial sums are
-added by the part that finishes last.  These tests run shapes where the
-schedule splits (checked through pgemm_schedule first, so a test cannot pass
-by not splitting) and compare with the oracle: bit-exact for int8 and for
+The tiles a partial last wave would hold have their K-iterations dealt out
+to the resident slots; the pieces of a tile meet through global memory and
+the last to finish adds them.  These tests run shapes where the schedule
+uses it (checked through pgemm_schedule first, so a test cannot pass by not
+splitting) and compare with the oracle: bit-exact for int8 and for
 integer-valued floats (a dropped, doubled or misplaced K range changes an
 exact integer), within 1e-4 * sqrt(K) * max|A| * max|B| for random bf16.  The
-fp32 sum of the parts is taken in part order, so repeated calls give the same
-bits however the parts finish.
+fp32 sum of the pieces is taken in slot order, so repeated calls give the
+same bits however the pieces finish.
 """
 import numpy as np
 import pytest
@@ -67,18 +67,36 @@ def check(orc, dtype, M, N, K, seed, kind="random", alpha=1, beta=0, config=None
     return got
 
 
-# K = 4100: 65 K-tiles, four 16-tile granules, so up to four parts, the last
-# one with the ragged 17th tile.
+# 1000 x 1000 x 4100: fewer tiles than slots for every configuration, so every
+# element of C comes from stream-K pieces: with the cap at 8, 65 K-tiles in
+# ranges of 13 to 27, up to six pieces a tile, the last piece of a tile
+# ending on the ragged 65th K-tile; with the default cap, equal halves.
+# Bit-exact against the oracle on sampled entries and against the same call
+# without stream-K on all of C.
 @pytest.mark.parametrize("dtype", ["bf16", "i8"])
-def test_every_config_splits_exactly(orc, dtype):
+def test_every_config_stream_k_exactly(orc, dtype):
+    M, N, K = 1000, 1000, 4100
+    A, B, C = operands(dtype, M, N, K, si.config_seed(20, 1 if dtype == "i8" else 2), "int")
+    one = 1 if dtype == "i8" else 1.0
+    zero = 0 if dtype == "i8" else 0.0
+    rng = np.random.default_rng(20)
+    ii = np.concatenate([np.arange(M), rng.integers(0, M, 3000), np.full(N, M - 1)])
+    jj = np.concatenate([np.arange(N), rng.integers(0, N, 3000), np.arange(N)])
+    ref = orc.entries(dtype, A, B, C, one, zero, ii, jj)
     for cfg in pg.pgemm_list_configs(dtype):
         if len(cfg) > 4:  # another producer or engine: not a persistent tensor-core kernel
             continue
-        M, N, K = (300, 200, 4100) if cfg[0] == 256 else (250, 260, 4100)
-        ok, s = splits(dtype, M, N, K, cfg)
-        assert ok, (cfg, s)
-        check(orc, dtype, M, N, K, si.config_seed(20, cfg[1] % 251 + cfg[3]), kind="int",
-              alpha=1 if dtype == "i8" else 1.0, beta=0 if dtype == "i8" else 0.0, config=cfg)
+        plain, status = run_gpu(dtype, A, B, C, one, zero, config=tuple(cfg) + (1,))
+        assert status == 0
+        assert np.array_equal(plain[ii, jj], ref.astype(plain.dtype)), cfg
+        for cap in (0, 8):
+            c = tuple(cfg) + (cap,)
+            ok, s = splits(dtype, M, N, K, c)
+            assert ok and s["split_tiles"] == s["tiles"], (c, s)
+            assert s["parts"] == 2 if cap == 0 else s["parts"] > 2, (c, s)
+            got, status = run_gpu(dtype, A, B, C, one, zero, config=c)
+            assert status == 0, (c, status)
+            assert np.array_equal(got, plain), c
 
 
 @pytest.mark.parametrize("max_parts", [2, 3, 8])
@@ -106,9 +124,9 @@ def test_random_bf16_within_bound_and_beta(orc):
 
 
 def test_int8_alpha_beta_wrap(orc):
-    ok, _ = splits("i8", 384, 512, 4096)
+    ok, _ = splits("i8", 384, 512, 8192)
     assert ok
-    check(orc, "i8", 384, 512, 4096, si.config_seed(23), alpha=-7, beta=3)
+    check(orc, "i8", 384, 512, 8192, si.config_seed(23), alpha=-7, beta=3)
 
 
 def test_bf16_repeat_bit_identical(orc):
@@ -153,12 +171,9 @@ def test_int8_exchange_stress(orc):
 
 
 def test_full_size_defaults_split():
-    """The bench's tensor-core workloads run with a split last wave when the
-    tiles leave it at most half full (on 152 SMs: int8 4096^3 and bf16 8192^3)."""
+    """The bench's tensor-core workloads deal their leftover tiles out (on 152
+    SMs: 28 of int8 4096^3's 256 pair tiles, 36 of bf16 8192^3's 1024)."""
     for dtype, n in (("i8", 4096), ("bf16", 8192)):
         s = pg.pgemm_schedule(dtype, n, n, n)
         rem = s["tiles"] % s["slots"]
-        if 0 < rem <= s["slots"] // 2:
-            assert s["split_tiles"] == rem and s["parts"] >= 2, s
-        else:
-            assert s["split_tiles"] == 0, s
+        assert rem > 0 and s["split_tiles"] == rem and 2 <= s["parts"] <= 8, s
