@@ -332,17 +332,20 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
     }
 
     // Operands as the kernels read them: element type, pitch, base pointer.
-    // int8 is widened to fp16, except for the mma.sync engine, which reads
-    // the int8 values with B transposed (N rows of K).
+    // int8 is widened to fp16 by a pre-pass, except for the mma.sync engine,
+    // which reads the int8 values with B transposed (N rows of K), and the
+    // register-staged producer, which reads them as they are (rows relaid
+    // out to 16-byte pitches when K or N is not a multiple of 16).
     const bool imma = KIND == Kind::I8 && k->engine == PGEMM_ENGINE_MMA_SYNC;
-    const int in_bytes = KIND == Kind::F32 ? 4 : (imma ? 1 : 2);
+    const bool rp = KIND == Kind::I8 && !imma && k->producer == PGEMM_PRODUCER_REGISTERS;
+    const int in_bytes = KIND == Kind::F32 ? 4 : ((imma || rp) ? 1 : 2);
     const long long lda = K, ldb = N;
     const void *a_op = A;
     const void *b_op = B;
     long long a_ld = lda, b_ld = ldb;
     Scratch scratch;
     scratch.s = stream;
-    Scratch split_area;  // partial sums and counters of K-split tiles
+    Scratch split_area;  // partial sums and counters of stream-K tiles
     split_area.s = stream;
     if (sched.split_tiles > 0) {
         const long long pbytes = round_up(sched.partial_words * 4, 256);
@@ -354,14 +357,14 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
         // The counters start at zero: the int8 widening pass (which the GEMM
         // waits for) zeroes them; otherwise a memset before any pre-pass does,
         // so that a programmatic launch after the pre-pass still finds them zero.
-        if (!(KIND == Kind::I8 && k->engine == PGEMM_ENGINE_DEFAULT && K > 0) &&
+        if (!(KIND == Kind::I8 && k->engine == PGEMM_ENGINE_DEFAULT && !rp && K > 0) &&
             cudaMemsetAsync(sched.counters, 0, cbytes, stream) != cudaSuccess)
             return PGEMM_ERR_CUDA;
     }
     std::function<cudaError_t()> prepass;  // repack / widening launch, if any
     if (K > 0) {
         const long long align_elems = 16 / in_bytes;
-        const bool widen = KIND == Kind::I8 && !imma;
+        const bool widen = KIND == Kind::I8 && !imma && !rp;
         const bool a_repack = widen || (lda * in_bytes) % 16 != 0;
         const bool b_repack = widen || imma || (ldb * in_bytes) % 16 != 0;
         if (a_repack || b_repack) {
@@ -383,14 +386,14 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
             // The pre-pass is launched below, after every tensor map is encoded,
             // so that the GEMM launch follows it with no host work in between.
             prepass = [=, &d]() -> cudaError_t {
-                if (imma) {  // A to a 16-byte pitch if needed; B -> B^T
+                if (imma || rp) {  // int8 to 16-byte pitches as needed; mma.sync: B -> B^T
                     cudaError_t e = cudaSuccess;
                     if (a_repack)
                         e = launch_i8_relayout(reinterpret_cast<const int8_t *>(A), lda, base,
                                                a_ld2, M, K, false, d->sm_count, stream);
-                    if (e == cudaSuccess)
+                    if (e == cudaSuccess && b_repack)
                         e = launch_i8_relayout(reinterpret_cast<const int8_t *>(B), ldb,
-                                               base + a_bytes, b_ld2, K, N, true, d->sm_count,
+                                               base + a_bytes, b_ld2, K, N, imma, d->sm_count,
                                                stream);
                     return e;
                 }
@@ -420,18 +423,19 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
         }
     }
 
-    // Tensor maps.  With K == 0 nothing is ever loaded; the maps then describe
-    // a 1 x 1 region of C so that they are still valid objects.
+    // Tensor maps.  With K == 0 nothing is ever loaded, nor by the
+    // register-staged producer; the maps then describe a 1 x 1 region of C so
+    // that they are still valid objects.
     alignas(64) CUtensorMap ta, tb;
     const CUtensorMapDataType tmt = KIND == Kind::F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                     : KIND == Kind::BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                    : imma               ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                    : (imma || rp)       ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     if (K > 0 && imma) {
         st = encode_2d(&ta, tmt, 1, a_op, K, M, a_ld, k->a_box_x, k->a_box_y, k->a_swizzle128);
         if (st == PGEMM_OK)  // B^T: N rows of K
             st = encode_2d(&tb, tmt, 1, b_op, K, N, b_ld, k->b_box_x, k->b_box_y, k->b_swizzle128);
-    } else if (K > 0) {
+    } else if (K > 0 && !rp) {
         st = encode_2d(&ta, tmt, in_bytes, a_op, K, M, a_ld, k->a_box_x, k->a_box_y, k->a_swizzle128);
         if (st == PGEMM_OK)
             st = encode_2d(&tb, tmt, in_bytes, b_op, N, K, b_ld, k->b_box_x, k->b_box_y,

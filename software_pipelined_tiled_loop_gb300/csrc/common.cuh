@@ -19,7 +19,7 @@ enum WaitSite : uint32_t {
     kSiteConvertFull = 7,     // int8 widening warps waiting for a staged int8 tile
     kSiteConvertEmpty = 8,    // int8 widening warps waiting for a free fp16 slot
     kSiteSelfTest = 9,        // pgemm_selftest_wait_timeout
-    kSiteSplitPartial = 10,   // last part of a K-split tile waiting for the others' partials
+    kSiteSplitPartial = 10,   // last piece of a stream-K tile waiting for the others' partials
 };
 
 // Problem description passed by value to every kernel.

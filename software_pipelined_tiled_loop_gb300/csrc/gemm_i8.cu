@@ -10,14 +10,18 @@
 // alpha*acc + beta*C modulo 2^32.  Bit-exact against the int64 oracle.
 //
 // The widening int8 -> fp16 is a separate, HBM-bound pass over A and B into
-// stream-ordered scratch (rows padded to 16-byte pitches for TMA); widening
-// inside the GEMM would put about three times the tensor core's own operand
-// traffic through shared memory.
+// stream-ordered scratch (rows padded to 16-byte pitches for TMA).  The CTA
+// pair kernels also exist with a register-staged producer that reads the
+// int8 operands itself and widens them on the way into the stage ring (the
+// LDG-to-register prefetch of the pages, PROD = 1); with one K-tile of loads
+// in flight per register buffer it runs at about a third of the TMA ring's
+// rate, so the TMA-fed kernel after the widening pass stays the default.
 #include <cuda_fp16.h>
 
 #include <vector>
 
 #include "tc_gemm.cuh"
+#include "widen.cuh"
 
 namespace pg {
 
@@ -25,14 +29,14 @@ constexpr int kI8ChunkTiles = 16;  // 16 K-tiles of 64 = 1024 products per exact
 
 // Each epilogue thread keeps a 128-column row of int32 sums in registers:
 // 128-wide tiles use four epilogue warps, 256-wide tiles eight.
-template <int BN, int STAGES, int CM = 1>
-using I8Cfg =
-    TcCfg<BN, STAGES, kI8ChunkTiles, /*BF16=*/0, /*INT_FOLD=*/true, BN == 256 ? 8 : 4, CM, CM>;
+template <int BN, int STAGES, int CM = 1, int PROD = 0>
+using I8Cfg = TcCfg<BN, STAGES, kI8ChunkTiles, /*BF16=*/0, /*INT_FOLD=*/true, BN == 256 ? 8 : 4,
+                    CM, CM, PROD>;
 
-template <int BN, int STAGES, int CM = 1>
+template <int BN, int STAGES, int CM = 1, int PROD = 0>
 static KernelInfo info_i8() {
-    KernelInfo k = tc_info<I8Cfg<BN, STAGES, CM>>();
-    k.launch_i8 = launch_tc<I8Cfg<BN, STAGES, CM>, LaunchI8>;
+    KernelInfo k = tc_info<I8Cfg<BN, STAGES, CM, PROD>>();
+    k.launch_i8 = launch_tc<I8Cfg<BN, STAGES, CM, PROD>, LaunchI8>;
     return k;
 }
 
@@ -44,6 +48,8 @@ const KernelInfo *i8_kernels(int *count) {
             info_i8<128, 2>(), info_i8<128, 3>(), info_i8<128, 4>(), info_i8<128, 5>(),
             info_i8<128, 6>(), info_i8<128, 1>(),
             info_i8<256, 4, 2>(), info_i8<256, 5, 2>(), info_i8<256, 6, 2>(),
+            // CTA pair with the register-staged producer (int8 read directly)
+            info_i8<256, 4, 2, 1>(), info_i8<256, 5, 2, 1>(), info_i8<256, 6, 2, 1>(),
         };
         int n = 0;
         const KernelInfo *imma = i8_imma_kernels(&n);
@@ -52,18 +58,6 @@ const KernelInfo *i8_kernels(int *count) {
     }();
     *count = static_cast<int>(table.size());
     return table.data();
-}
-
-// Exact int8 -> fp16 for four packed bytes: bias each byte to b = x + 128,
-// place it under the fp16 exponent 0x64 (the fp16 value 1024 + b, exact), and
-// subtract 1152 with one half2 op: 1024 + x + 128 - 1152 = x, exact.
-__device__ __forceinline__ void widen4(uint32_t w, __half2 &lo, __half2 &hi) {
-    const uint32_t b = w ^ 0x80808080u;                    // x + 128 per byte
-    const uint32_t l = __byte_perm(b, 0x64646464u, 0x4140);  // [0x64 b1 | 0x64 b0]
-    const uint32_t h = __byte_perm(b, 0x64646464u, 0x4342);  // [0x64 b3 | 0x64 b2]
-    const __half2 bias = __half2half2(__ushort_as_half(0x6480));  // 1152.0
-    lo = __hsub2(*reinterpret_cast<const __half2 *>(&l), bias);
-    hi = __hsub2(*reinterpret_cast<const __half2 *>(&h), bias);
 }
 
 struct WidenJob {
@@ -90,7 +84,7 @@ constexpr int kWidenGroups = 2;
 
 __global__ void __launch_bounds__(256, 6) widen_i8_to_f16_kernel(WidenJob ja, WidenJob jb,
                                                                  uint32_t *zero, int zero_words) {
-    // the GEMM's K-split tickets start at zero (it reads them only after this
+    // the GEMM's stream-K tickets start at zero (it reads them only after this
     // grid has completed)
     if (blockIdx.x == 0 && blockIdx.y == 0)
         for (int i = threadIdx.x; i < zero_words; i += blockDim.x) zero[i] = 0u;

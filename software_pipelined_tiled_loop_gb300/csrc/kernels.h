@@ -88,9 +88,10 @@ struct KernelInfo {
     // launch; nullptr for kernels with one block per tile.
     int kc = 0;
     int slabs_per_tile = 0;  // epilogue warps per tile (all CTAs of a pair)
-    // FFMA kernels: the leftover tiles' K-iterations are dealt out to all
-    // slots by a head grid (aux_func) before the whole tiles, instead of
-    // K-splitting whole tiles.
+    // FFMA kernels: the stream-K pieces run as a second grid (aux_func)
+    // behind the whole tiles, one ticket per leftover tile and no default cap
+    // on pieces; the tensor-core kernels run them in-kernel, two counters per
+    // tile and epilogue warp, at most two pieces a tile by default.
     bool stream_k = false;
     cudaError_t (*schedule_slots)(const LaunchCommon &, int *slots) = nullptr;
     const void *func = nullptr;

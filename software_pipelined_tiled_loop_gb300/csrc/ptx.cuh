@@ -107,6 +107,35 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
     }
 }
 
+// The same wait with acquire semantics at cluster scope: for a barrier that
+// threads of the peer CTA arrive on (release.cluster) after writing shared
+// memory that this CTA's tensor-core operations then read.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity,
+                                                  const KernelCtx &ctx, uint32_t site) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > ctx.wait_limit_ns) {
+            atomicCAS(ctx.status, 0u, kStatusTimeout | (site & 0xffffu));
+            return false;
+        }
+    }
+}
+
 // Has any block of this grid (or an earlier launch) recorded a failure?
 __device__ __forceinline__ bool device_failed(const KernelCtx &ctx) {
     return *reinterpret_cast<volatile uint32_t *>(ctx.status) != 0u;
@@ -421,6 +450,27 @@ __device__ __forceinline__ bool wait_counter(const uint32_t *p, uint32_t target,
 
 // ------------------------------------------------------------ misc utils ---
 __device__ __forceinline__ bool elect_lane0() { return (threadIdx.x & 31u) == 0u; }
+
+// Per-thread register allotment of the executing warpgroup (all four warps
+// execute the same instruction): dec returns registers to the block's pool,
+// inc waits until the pool can grant them.  The block's pool is what it was
+// launched with (threads x registers at launch), so the warpgroups' shares
+// must add up to no more than that.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg count");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg count");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// 16-byte read-only global load.
+__device__ __forceinline__ uint4 ldg_nc_v4(const void *p) {
+    return __ldg(reinterpret_cast<const uint4 *>(p));
+}
 
 // Named barrier over `nthreads` threads (a multiple of 32), id 1..15.
 __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t nthreads) {

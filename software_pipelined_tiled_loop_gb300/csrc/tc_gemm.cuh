@@ -54,6 +54,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
+#include "widen.cuh"
 
 namespace pg {
 
@@ -66,8 +67,15 @@ namespace pg {
 // even CTA; each CTA loads and holds its 128 rows of A and half of B's
 // columns (so a stage is a third smaller and the ring one to two stages
 // deeper), and receives its 128 rows of the accumulator in its own TMEM.
+// PROD: who fills the stage ring.  0: one lane of warp 0 issues TMA copies.
+// 1: four producer warps (warps 0-3) load int8 A and B tiles from global
+// memory into registers, widen them to fp16 there and store them into the
+// swizzled stage; the separate widening pass disappears.  Then the
+// epilogue warps are 4 .. 4 + EPI - 1 and the MMA issuer is warp 4 + EPI,
+// and every role is a whole warpgroup, so that setmaxnreg can move
+// registers from the producers and the MMA warpgroup to the epilogue.
 template <int BN_, int STAGES_, int KC_, int BF16_, bool INT_FOLD_, int EPI_ = 4, int CM_ = 1,
-          int CG_ = 1>
+          int CG_ = 1, int PROD_ = 0>
 struct TcCfg {
     static constexpr int BM = 128, BN = BN_, BK = 64, STAGES = STAGES_, KC = KC_, CM = CM_;
     static constexpr int CG = CG_;
@@ -88,7 +96,15 @@ struct TcCfg {
     static constexpr int STAGING_BYTES = EPI * STAGE_BUFS * 32 * 32 * 4;
     static constexpr int ACC_COLS = BN;        // fp32 accumulator: one TMEM column per n
     static constexpr int TMEM_COLS = 2 * BN;   // two accumulators
-    static constexpr int THREADS = 64 + 32 * EPI;
+    static constexpr int PROD = PROD_;
+    static constexpr int EPI_WARP0 = PROD ? 4 : 2;        // first epilogue warp
+    static constexpr int MMA_WARP = PROD ? 4 + EPI : 1;   // MMA issuer, owns TMEM
+    static constexpr int THREADS = PROD ? 32 * (4 + EPI + 4) : 64 + 32 * EPI;
+    // arrivals that complete a stage's full barrier: the TMA producer's
+    // expect_tx, or one per producer warp of each CTA
+    static constexpr int FULL_ARRIVALS = PROD ? 4 * CG : 1;
+    // setmaxnreg shares of the PROD = 1 layout (launched at 65536 / THREADS)
+    static constexpr int REGS_PRODUCER = 104, REGS_MMA = 48, REGS_EPILOGUE = 176;
     static constexpr int STAGING_OFFSET = STAGES * STAGE_BYTES;
     static constexpr int BAR_OFFSET = STAGING_OFFSET + STAGING_BYTES;
     static constexpr int NUM_BARS = 2 * STAGES + 5;
@@ -106,6 +122,11 @@ struct TcCfg {
     static_assert(USED + 1024 <= 232448, "shared memory");
     static_assert((CM == 1 && CG == 1) || (CM == 2 && CG == 2 && (BN / 64) % 2 == 0),
                   "a CTA pair is a cluster of two splitting B's columns in halves");
+    static_assert(!PROD || (INT_FOLD && EPI == 8 && B_COLS % 128 == 0),
+                  "register-staged producer: int8 operands, two epilogue warpgroups");
+    static_assert(!PROD || 128 * (REGS_PRODUCER + REGS_MMA) + 32 * EPI * REGS_EPILOGUE <=
+                               65536, "setmaxnreg shares exceed the block's registers");
+    static_assert(!PROD || THREADS == 512, "launched at 128 registers a thread");
 };
 
 // One warp writes a 32 x 32 block of C: rows [m_base, m_base + 32), columns
@@ -388,13 +409,134 @@ struct SplitSlab {
     }
 };
 
+// The int8 operands as stored by the caller, for the register-staged
+// producer: row-major, pitches in elements (bytes), rows 16-byte aligned.
+struct TcOperands {
+    const int8_t *A;
+    const int8_t *B;
+    long long lda, ldb;
+};
+
+// Register-staged int8 producer (PROD = 1), run by the 128 threads of warps
+// 0-3 of each CTA.  For every K-tile of the slot's units it loads this CTA's
+// 128 x 64 slice of A and 64 x B_COLS slice of B from global memory (16-byte
+// vectors, zero outside the matrices), widens the bytes to fp16 exactly in
+// registers and stores them into the stage with the same 128-byte swizzle a
+// TMA copy would produce, so the MMA issuer's descriptors are unchanged.  The
+// loads of the next K-tile are issued before the current one is converted
+// (the register double buffer of the pages' LDG-to-register prefetch), and
+// the stage ring in front of the MMA issuer is S deep as before.  Each warp
+// fences its stores into the async proxy and arrives once on the stage's full
+// barrier (with a CTA pair: the even CTA's, released at cluster scope).
+//
+// Thread t's share of a K-tile, chosen so that each 8-lane phase of a
+// 16-byte shared store covers 32 distinct banks and each warp load covers
+// whole 64-byte row segments:
+//   A: rows (t >> 2) + 32 p, p < 4, byte chunk t & 3 of the row's 64 bytes;
+//   B: rows 16 r + 4 w + ((l >> 2) & 1) + 2 ((l >> 4) & 1), r < 4, of the
+//      column panel 2 h + ((l >> 3) & 1), h < B_COLS / 128, byte chunk l & 3
+//      of the panel's 64 bytes (w = t >> 5, l = t & 31).
+// v with its bytes n .. 15 cleared (0 < n < 16): a vector that straddles the
+// end of a row (the padding of a relaid-out operand holds no values).
+__device__ __forceinline__ uint4 keep_bytes(uint4 v, int n) {
+    auto m = [n](int i) -> uint32_t {
+        const int k = n - 4 * i;
+        return k >= 4 ? 0xffffffffu : (k <= 0 ? 0u : (1u << (8 * k)) - 1u);
+    };
+    v.x &= m(0);
+    v.y &= m(1);
+    v.z &= m(2);
+    v.w &= m(3);
+    return v;
+}
+
+template <class Cfg>
+struct RegProducer {
+    static constexpr int BK = Cfg::BK, BM = Cfg::BM;
+    static constexpr int NB = 4 * (Cfg::B_COLS / 128);  // B vectors per thread per K-tile
+    // One K-tile's vectors as loaded, and how many bytes of each A vector and
+    // of each B panel pair's vectors lie inside the matrix (the bytes past the
+    // end are cleared when the tile is stored, not when it is loaded, so that
+    // nothing waits for a load before the tile is needed).
+    struct Tile {
+        uint4 a[4], b[NB];
+        int an, bn[NB / 4];
+    };
+
+    int a_row, a_col, b_row, b_col;   // this thread's base coordinates within a tile
+    uint32_t a_soff, b_soff;          // its swizzled byte offsets within a stage (chunk 2q)
+    uint32_t a_x, b_x;                // the row's swizzle (row & 7)
+
+    __device__ __forceinline__ explicit RegProducer(uint32_t t) {
+        const uint32_t w = t >> 5, l = t & 31u;
+        a_row = static_cast<int>(t >> 2);
+        a_col = static_cast<int>(t & 3u) * 16;
+        a_x = (t >> 2) & 7u;
+        a_soff = (t >> 2) * 128u;
+        b_row = static_cast<int>(4 * w + ((l >> 2) & 1u) + 2 * ((l >> 4) & 1u));
+        b_col = static_cast<int>(((l >> 3) & 1u) * 64 + (l & 3u) * 16);
+        b_x = static_cast<uint32_t>(b_row) & 7u;
+        b_soff = ((l >> 3) & 1u) * (BK * 128) + static_cast<uint32_t>(b_row) * 128u;
+    }
+
+    // Issue the loads of K-tile kt for the tile whose A rows start at m0 and
+    // whose B columns (this CTA's share) start at nb.  Rows are 16-byte
+    // aligned and padded to a multiple of 16 bytes, so a vector that starts
+    // inside a row is readable whole.  Vectors outside the matrix are zero.
+    __device__ __forceinline__ void load(Tile &t, const TcOperands &op, int M, int N, int K,
+                                         int m0, int nb, int kt) const {
+        const int k0 = kt * BK;
+        t.an = K - (k0 + a_col);  // bytes of A's vectors inside the K range
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const int r = m0 + a_row + 32 * p;
+            t.a[p] = make_uint4(0u, 0u, 0u, 0u);
+            if (r < M && t.an > 0)
+                t.a[p] = ldg_nc_v4(op.A + static_cast<long long>(r) * op.lda + (k0 + a_col));
+        }
+#pragma unroll
+        for (int h = 0; h < NB / 4; ++h) t.bn[h] = N - (nb + b_col + 128 * h);
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+            const int kr = k0 + b_row + 16 * (i & 3);
+            const int c = nb + b_col + 128 * (i >> 2);
+            t.b[i] = make_uint4(0u, 0u, 0u, 0u);
+            if (kr < K && c < N) t.b[i] = ldg_nc_v4(op.B + static_cast<long long>(kr) * op.ldb + c);
+        }
+    }
+
+    // Widen and store the loaded K-tile into the stage at shared addresses
+    // sa (A) and sb (B).
+    __device__ __forceinline__ void store(const Tile &t, uint32_t sa, uint32_t sb) const {
+        const uint32_t qa = static_cast<uint32_t>(a_col) >> 3;         // 2 q
+        const uint32_t qb = (static_cast<uint32_t>(b_col) & 63u) >> 3;  // 2 q within the panel
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            uint32_t o[8];
+            widen16(t.an < 16 && t.an > 0 ? keep_bytes(t.a[p], t.an) : t.a[p], o);
+            const uint32_t base = sa + a_soff + 4096u * p;
+            sts128(base + ((qa ^ a_x) << 4), o[0], o[1], o[2], o[3]);
+            sts128(base + (((qa + 1) ^ a_x) << 4), o[4], o[5], o[6], o[7]);
+        }
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+            uint32_t o[8];
+            const int bn = t.bn[i >> 2];
+            widen16(bn < 16 && bn > 0 ? keep_bytes(t.b[i], bn) : t.b[i], o);
+            const uint32_t base = sb + b_soff + 2048u * (i & 3) + 2u * BK * 128u * (i >> 2);
+            sts128(base + ((qb ^ b_x) << 4), o[0], o[1], o[2], o[3]);
+            sts128(base + (((qb + 1) ^ b_x) << 4), o[4], o[5], o[6], o[7]);
+        }
+    }
+};
+
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b,
                    const __grid_constant__ CUtensorMap tmap_c,
                    const GemmArgs<typename Cfg::Scalar, typename Cfg::Scalar> args,
-                   const KernelCtx ctx) {
+                   const TcOperands ops, const KernelCtx ctx) {
     using Scalar = typename Cfg::Scalar;
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -419,11 +561,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     if (warp == 0 && lane == 0) {
         sp.init(args, static_cast<int>(blockIdx.x) / Cfg::CM, static_cast<int>(gridDim.x) / Cfg::CM,
                 num_m_sched * args.num_n_tiles);
-        prefetch_tmap(&tmap_a);
-        prefetch_tmap(&tmap_b);
+        if constexpr (!Cfg::PROD) {
+            prefetch_tmap(&tmap_a);
+            prefetch_tmap(&tmap_b);
+        }
         if (args.c_tma) prefetch_tmap(&tmap_c);
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], Cfg::FULL_ARRIVALS);
             // released by the MMA issuer (with a CTA pair: the even CTA's, whose
             // MMAs read this CTA's stage too)
             mbar_init(&empty[s], 1);
@@ -436,7 +580,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         mbar_init(mma_done, 1);
         fence_barrier_init();
     }
-    if (warp == 1) {
+    if (warp == Cfg::MMA_WARP) {
         if constexpr (Cfg::CG == 2) {
             tmem_alloc_pair(tmem_slot, Cfg::TMEM_COLS);  // both CTAs; same address in each
             tmem_relinquish_pair();
@@ -460,8 +604,74 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     const uint32_t crank = Cfg::CM > 1 ? cluster_ctarank() : 0u;
     const int num_units = sp.units();
 
-    if (warp == 0) {
-        if (lane == 0) {
+    if (Cfg::PROD ? warp < 4 : warp == 0) {
+        if constexpr (Cfg::PROD) {
+            // ------- producer: int8 loads widened in registers (warps 0-3) -------
+            setmaxnreg_dec<Cfg::REGS_PRODUCER>();
+            const RegProducer<Cfg> rp(threadIdx.x);
+            using Tile = typename RegProducer<Cfg>::Tile;
+            Tile x, y;  // two K-tiles in registers, used in turn
+            // The slot's K-tiles in order: unit u, K-tile kt < ke, and the
+            // unit's A row and B column origins for this CTA.
+            int u = -1, kt = -1, ke = 0, m0 = 0, nb = 0;
+            auto advance = [&](int &uu, int &k, int &kend, int &m, int &n) -> bool {
+                ++k;
+                while (k >= kend) {
+                    if (++uu >= num_units) return false;
+                    const WorkUnit w = sp.unit(uu);
+                    k = w.kb;
+                    kend = w.ke;
+                    tile_origin(w.tile, num_m_sched, args.num_n_tiles, args.group_m,
+                                BM * Cfg::CM, BN, m, n);
+                    m += static_cast<int>(crank) * BM;
+                    n += static_cast<int>(crank) * Cfg::B_COLS;
+                }
+                return true;
+            };
+            uint32_t it = 0;
+            bool ok = true;
+            // Store the K-tile held in `now` into the next stage; before that,
+            // issue the loads of the one after it into `next`.  Returns
+            // whether there is a next one.
+            auto step = [&](Tile &now, Tile &next) -> bool {
+                int u2 = u, kt2 = kt, ke2 = ke, m2 = m0, n2 = nb;
+                const bool have2 = advance(u2, kt2, ke2, m2, n2);
+                if (have2) rp.load(next, ops, args.M, args.N, args.K, m2, n2, kt2);
+                const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+                if (lane == 0) ok = mbar_wait(&empty[s], ph ^ 1u, ctx, kSiteProducerEmpty);
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                if (!ok) return false;
+                rp.store(now, smem_u32(sA + s * Cfg::A_BYTES), smem_u32(sB + s * Cfg::B_BYTES));
+                // the stores become visible to the tensor core's reads, then
+                // one arrival per warp
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (Cfg::CG == 2)
+                        mbar_arrive_cluster(mapa_shared(smem_u32(&full[s]), 0));
+                    else
+                        mbar_arrive(&full[s]);
+                }
+                ++it;
+                u = u2;
+                kt = kt2;
+                ke = ke2;
+                m0 = m2;
+                nb = n2;
+                return have2;
+            };
+            bool have = advance(u, kt, ke, m0, nb);
+            if (have) rp.load(x, ops, args.M, args.N, args.K, m0, nb, kt);
+            while (have && step(x, y)) have = step(y, x);
+            if constexpr (Cfg::CM > 1) {
+                // as below: the last multicast releases land before the exit
+                if (threadIdx.x == 0)
+                    for (int i = 0; ok && i < STAGES; ++i, ++it) {
+                        const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+                        ok = mbar_wait(&empty[s], ph ^ 1u, ctx, kSiteProducerEmpty);
+                    }
+            }
+        } else if (lane == 0) {
             // ---------------- producer: TMA into the stage ring ----------------
             uint32_t it = 0;
             bool ok = true;
@@ -510,9 +720,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 }
             }
         }
-    } else if (warp == 1) {
+    } else if (Cfg::PROD ? warp >= static_cast<uint32_t>(Cfg::MMA_WARP) : warp == 1) {
+        if constexpr (Cfg::PROD) setmaxnreg_dec<Cfg::REGS_MMA>();  // the MMA warpgroup
         // with a CTA pair only the even CTA issues (its MMAs cover both CTAs)
-        if (lane == 0 && (Cfg::CG == 1 || crank == 0)) {
+        if (warp == Cfg::MMA_WARP && lane == 0 && (Cfg::CG == 1 || crank == 0)) {
             // ---------------- MMA issuer ----------------
             constexpr uint32_t idesc = idesc_f16(BM * Cfg::CG, BN, Cfg::BF16, /*A K-major*/ 0,
                                                  /*B N-major*/ 1);
@@ -535,7 +746,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     const int k_end = min(w.ke, k_begin + kct);
                     for (int kt = k_begin; kt < k_end; ++kt, ++it) {
                         const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-                        if (!mbar_wait(&full[s], ph, ctx, kSiteMmaFull)) {
+                        // register-staged stages of a pair: the odd CTA's warps
+                        // released their stores at cluster scope
+                        const bool landed = (Cfg::PROD && Cfg::CG == 2)
+                                                ? mbar_wait_cluster(&full[s], ph, ctx, kSiteMmaFull)
+                                                : mbar_wait(&full[s], ph, ctx, kSiteMmaFull);
+                        if (!landed) {
                             ok = false;
                             break;
                         }
@@ -576,7 +792,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         }
     } else {
         // ---------------- epilogue warps ----------------
-        const uint32_t e = warp - 2;            // epilogue warp index
+        if constexpr (Cfg::PROD) setmaxnreg_inc<Cfg::REGS_EPILOGUE>();
+        const uint32_t e = warp - Cfg::EPI_WARP0;  // epilogue warp index
         const uint32_t q = warp & 3u;           // the TMEM lane quadrant this warp may read
         const int col0 = static_cast<int>(e >> 2) * Cfg::EPI_COLS;  // its column range
         uint8_t *wbuf = sStage + e * (Cfg::STAGE_BUFS * 32 * 32 * 4);  // this warp's buffers
@@ -681,7 +898,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     tc_fence_after();
                     const uint32_t t_row =
                         tmem_base + ((q * 32u) << 16) + ab * Cfg::ACC_COLS + col0;
-                    // role in a K-split tile: store a partial, or add them all
+                    // role in a stream-K tile: store a partial, or add them all
                     int role = 0;  // 0: whole tile, 1: store partial, 2: reduce
                     SplitSlab<Cfg> slab = split ? SplitSlab<Cfg>(args, sp, w, crank, e) : SplitSlab<Cfg>();
                     if (split) {
@@ -734,7 +951,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         cluster_sync();  // no CTA leaves while its peer may still signal it
     else
         __syncthreads();
-    if (warp == 1) {
+    if (warp == Cfg::MMA_WARP) {
         __syncwarp();
         tc_fence_after();
         if constexpr (Cfg::CG == 2)
@@ -796,7 +1013,25 @@ static cudaError_t launch_tc(const P &p, cudaStream_t stream) {
         ++nattr;
     }
     lc.numAttrs = nattr;
-    return cudaLaunchKernelEx(&lc, tc_gemm_kernel<Cfg>, *p.tmap_a, *p.tmap_b, tc, a, p.ctx);
+    TcOperands ops{};
+    if constexpr (Cfg::PROD) {
+        // setmaxnreg.inc waits until the block's pool can grant the
+        // registers, and the pool is what the kernel was launched with:
+        // launch only if the shares fit it, so that no warpgroup can wait
+        // for registers that will never come.
+        static const bool regs_fit = [] {
+            cudaFuncAttributes fa{};
+            return cudaFuncGetAttributes(&fa, tc_gemm_kernel<Cfg>) == cudaSuccess &&
+                   fa.numRegs * Cfg::THREADS >= 128 * (Cfg::REGS_PRODUCER + Cfg::REGS_MMA) +
+                                                    32 * Cfg::EPI * Cfg::REGS_EPILOGUE;
+        }();
+        if (!regs_fit) return cudaErrorInvalidConfiguration;
+        ops.A = static_cast<const int8_t *>(p.a_ptr);
+        ops.B = static_cast<const int8_t *>(p.b_ptr);
+        ops.lda = p.lda;
+        ops.ldb = p.ldb;
+    }
+    return cudaLaunchKernelEx(&lc, tc_gemm_kernel<Cfg>, *p.tmap_a, *p.tmap_b, tc, a, ops, p.ctx);
 }
 
 // Schedule slots of a persistent launch: resident CTAs (at most MAX_BLOCKS per
@@ -845,6 +1080,7 @@ static KernelInfo tc_info() {
     k.c_tma = true;
     k.kc = Cfg::KC;
     k.slabs_per_tile = Cfg::CM * Cfg::EPI;
+    k.producer = Cfg::PROD ? PGEMM_PRODUCER_REGISTERS : PGEMM_PRODUCER_TMA;
     k.schedule_slots = tc_slots<Cfg>;
     k.func = reinterpret_cast<const void *>(tc_gemm_kernel<Cfg>);
     return k;

@@ -62,7 +62,11 @@ def test_list_configs(L):
     # the register-staged comparator: fp32 only, two buffers, named by its producer
     regs = [c for c in f32 if len(c) > 5 and c[5] == pg.PRODUCERS["registers"]]
     assert {(c[0], c[1], c[3]) for c in regs} == {(128, 128, 2), (128, 64, 2)}
-    assert not [c for c in bf16 + i8 if len(c) > 5 and c[5] != pg.PRODUCERS["tma"]]
+    assert not [c for c in bf16 if len(c) > 5 and c[5] != pg.PRODUCERS["tma"]]
+    # int8 on the CTA pair also with the register-staged producer (int8 read
+    # and widened in registers by the GEMM itself)
+    i8_regs = [c for c in i8 if len(c) > 5 and c[5] == pg.PRODUCERS["registers"]]
+    assert {(c[0], c[1], c[3]) for c in i8_regs} == {(256, 256, 4), (256, 256, 5), (256, 256, 6)}
     # the mma.sync int8 engine: 128 x 128 tiles, K-tiles of 128 int8
     imma = [c for c in i8 if len(c) > 6 and c[6] == pg.ENGINES["mma_sync"]]
     assert {(c[0], c[1], c[2]) for c in imma} == {(128, 128, 128)}
