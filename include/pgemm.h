@@ -24,11 +24,15 @@
  *   - The call is asynchronous on `stream` (NULL = the legacy default
  *     stream): it enqueues work and returns; the caller synchronises.  The
  *     library may enqueue a small repack kernel and stream-ordered scratch
- *     (cudaMallocAsync / cudaFreeAsync) on the same stream when a leading
- *     dimension is not a multiple of 16 bytes, and stream-ordered scratch
- *     for partial sums when tiles are split along K (see
+ *     on the same stream when a leading dimension is not a multiple of 16
+ *     bytes (int8: its widened operands), and stream-ordered scratch for
+ *     partial sums when tiles are split along K (see
  *     pgemm_config.max_k_parts), whose counters a cudaMemsetAsync zeroes
- *     (int8: its widening kernel does).
+ *     (int8: its widening kernel does).  Scratch comes from a memory pool
+ *     the library owns per device (cudaMallocFromPoolAsync /
+ *     cudaFreeAsync) that keeps the memory it has mapped, so that calls
+ *     with synchronisations between them do not map it again;
+ *     pgemm_trim_scratch() gives it back.
  *   - M, N, K >= 0.  M == 0 or N == 0: nothing is done.  K == 0: C <- beta*C
  *     (C is not read when beta == 0, so a NaN in C does not survive).
  *   - beta == 0: C is not read (BLAS convention).
@@ -264,6 +268,11 @@ PGEMM_API pgemm_status pgemm_selftest_wait_timeout(int limit_us, pgemm_stream_t 
 
 /* A static description of a status code. */
 PGEMM_API const char *pgemm_status_string(pgemm_status status);
+
+/* Synchronises the current device, then returns all unused memory of the
+ * library's scratch pool on it to the system (the pool keeps what it has
+ * mapped between calls otherwise).  PGEMM_ERR_CUDA on a CUDA error. */
+PGEMM_API pgemm_status pgemm_trim_scratch(void);
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 PGEMM_API int pgemm_version(void);

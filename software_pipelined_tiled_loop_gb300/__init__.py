@@ -20,7 +20,7 @@ __all__ = [
     "gemm_bf16_ex", "gemm_i8_ex", "pgemm_default_config", "pgemm_list_configs",
     "pgemm_kernel_attrs", "pgemm_get_device_status", "pgemm_selftest_wait_timeout",
     "pgemm_status_string", "pgemm_version", "gemm_i8_noalloc", "NOALLOC_SCRATCH_BYTES",
-    "pgemm_stage_reuse_demo", "pgemm_schedule", "pgemm_stream_k_plan",
+    "pgemm_stage_reuse_demo", "pgemm_schedule", "pgemm_stream_k_plan", "pgemm_trim_scratch",
     "DTYPES", "STATUS", "EXPORTED", "PRODUCERS", "ENGINES",
 ]
 
@@ -45,7 +45,7 @@ EXPORTED = [
     "pgemm_default_config", "pgemm_list_configs", "pgemm_kernel_attrs",
     "pgemm_get_device_status", "pgemm_selftest_wait_timeout", "pgemm_status_string",
     "pgemm_version", "gemm_i8_noalloc", "pgemm_stage_reuse_demo", "pgemm_schedule",
-    "pgemm_stream_k_plan",
+    "pgemm_stream_k_plan", "pgemm_trim_scratch",
 ]
 
 
@@ -102,6 +102,7 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
         "pgemm_stage_reuse_demo": [vp, i, i, vp, vp, i, i, ctypes.c_uint, vp, i, vp],
         "pgemm_schedule": [i, cfgp, i, i, i, llp, ip, llp, ip],
         "pgemm_stream_k_plan": [ll, i, i, i, llp, ip, ip, llp],
+        "pgemm_trim_scratch": [],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -278,3 +279,9 @@ def pgemm_status_string(code: int) -> str:
 
 def pgemm_version() -> int:
     return int(lib().pgemm_version())
+
+
+def pgemm_trim_scratch() -> None:
+    """Synchronise the current device and give the library's unused scratch
+    memory back (the pool otherwise keeps it between calls)."""
+    _check(lib().pgemm_trim_scratch(), "pgemm_trim_scratch")

@@ -177,3 +177,23 @@ def test_full_size_defaults_split():
         s = pg.pgemm_schedule(dtype, n, n, n)
         rem = s["tiles"] % s["slots"]
         assert rem > 0 and s["split_tiles"] == rem and 2 <= s["parts"] <= 8, s
+
+
+def test_scratch_pool_trim_and_reuse(orc):
+    """Scratch (partial sums, counters, widened int8) comes from the library's
+    own pool, which keeps its memory across synchronisations; after
+    pgemm_trim_scratch gives it back, the next calls map it again and stay
+    bit-exact, with the stream-K counters zero at every launch."""
+    M, N, K = 1000, 1000, 4100
+    for dtype in ("i8", "bf16"):
+        ok, _ = splits(dtype, M, N, K)
+        assert ok
+        kind = "random" if dtype == "i8" else "int"
+        A, B, C = operands(dtype, M, N, K, si.config_seed(26), kind)
+        ref = orc.gemm(dtype, A, B, C, 1, 0)
+        for trim in (False, True, False):
+            if trim:
+                pg.pgemm_trim_scratch()
+            got, status = run_gpu(dtype, A, B, C, 1, 0)
+            assert status == 0
+            compare(dtype, got, ref, A, B, K, exact=True)
