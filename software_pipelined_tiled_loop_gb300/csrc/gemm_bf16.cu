@@ -5,14 +5,16 @@
 
 namespace pg {
 
-// 256-wide tiles use eight epilogue warps (two per TMEM lane quadrant), so a
-// tile's epilogue takes half as long; 128-wide tiles keep four, which leaves
-// room for two resident blocks per SM at shallow rings.
+// Eight epilogue warps (two per TMEM lane quadrant, each half the columns),
+// so a tile's epilogue takes half as long as with four: at short K the calls
+// are bound by the epilogue (a warp stages and stores its 32-column blocks
+// one after another).  128-wide tiles with one or two stages keep four,
+// which leaves room for two resident blocks per SM.
 // CM = CG = 2: a CTA pair computes a 256 x BN tile with one M = 256 MMA (each
 // CTA holds half of A's rows and half of B's columns), listed as bm = 256.
 template <int BN, int STAGES, int CM = 1>
-using Bf16Cfg =
-    TcCfg<BN, STAGES, /*KC=*/0, /*BF16=*/1, /*INT_FOLD=*/false, BN == 256 ? 8 : 4, CM, CM>;
+using Bf16Cfg = TcCfg<BN, STAGES, /*KC=*/0, /*BF16=*/1, /*INT_FOLD=*/false,
+                      (BN == 256 || STAGES >= 3) ? 8 : 4, CM, CM>;
 
 template <int BN, int STAGES, int CM = 1>
 static KernelInfo info_bf16() {
