@@ -82,15 +82,21 @@ typedef enum { PGEMM_F32 = 0, PGEMM_BF16 = 1, PGEMM_I8 = 2 } pgemm_dtype;
  *   PGEMM_PRODUCER_TMA: TMA bulk-tensor copies into an S-stage ring guarded by
  *     full / empty mbarriers, issued by one producer thread (every dtype; the
  *     default).
- *   PGEMM_PRODUCER_REGISTERS (fp32 only, stages = 2): the comparator of
- *     "GPU-Kernel pipelinen" (step 3, the LDG-register variant) and of the
- *     double-buffered SGEMM of "Double Buffering: Software Pipelining the
- *     K-Loop" (section "The Kernel"): every thread of the block loads its
- *     share of K-tile t+1 from global memory into registers while the block
- *     computes tile t from one of two shared-memory buffers, then stores the
- *     registers into the other buffer, and one block barrier per K-tile hands
- *     the buffers over.  Same tile, register tile and arithmetic as the TMA
- *     kernel; only the producer differs. */
+ *   PGEMM_PRODUCER_REGISTERS: the comparator of "GPU-Kernel pipelinen"
+ *     (step 3, the LDG-register variant) and of the double-buffered SGEMM of
+ *     "Double Buffering: Software Pipelining the K-Loop" (section "The
+ *     Kernel"), threads loading the next K-tile into registers:
+ *     - fp32 (128 x 128 and 128 x 64, stages = 2): every thread of the block
+ *       loads its share of K-tile t+1 while the block computes tile t from
+ *       one of two shared-memory buffers, then stores the registers into the
+ *       other buffer, and one block barrier per K-tile hands the buffers
+ *       over.  Same tile, register tile and arithmetic as the TMA kernel;
+ *       only the producer differs.
+ *     - int8 (CTA pair 256 x 256, stages 4..6): four producer warps per CTA
+ *       load the int8 tiles, widen them exactly to fp16 in registers and
+ *       store them into the S-stage ring the tensor core reads, so no
+ *       widening pass runs; the MMA issuer and the exact-round epilogue are
+ *       the default kernel's. */
 typedef enum { PGEMM_PRODUCER_TMA = 0, PGEMM_PRODUCER_REGISTERS = 1 } pgemm_producer;
 
 /* Which multiply-accumulate consumes the stages (pgemm_config.engine).
