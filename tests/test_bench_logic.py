@@ -82,3 +82,12 @@ def test_workloads_match_the_metric_shapes():
     assert bench.WORKLOADS["igemm_i8_4096"][:4] == ("i8", 4096, 4096, 4096)
     assert bench.WORKLOADS["gemm_bf16_8192"][:4] == ("bf16", 8192, 8192, 8192)
     assert bench.L2_FLUSH_BYTES > 129 * 10 ** 6
+
+
+def test_vs_baseline_uses_the_pages_figure_only_where_they_print_one():
+    # the SGEMM page: 2 * 4096^3 FLOP in 4.281 ms = 32.1075 TFLOP/s
+    assert bench.PAGE_FIGURES["sgemm_fp32_4096"][0] == pytest.approx(2 * 4096 ** 3 / 4.281e-3 / 1e12,
+                                                                      rel=1e-4)
+    assert bench.vs_baseline("sgemm_fp32_4096", 64.215) == pytest.approx(2.0, abs=1e-3)
+    assert bench.vs_baseline("gemm_bf16_8192", 1800.0) is None
+    assert bench.vs_baseline("igemm_i8_4096", 1280.0) is None
