@@ -101,6 +101,12 @@ def roofline_for(dtype: str, achieved_tflops: float, sm_count: int, peaks: dict)
            "frac": round(achieved_tflops / peak, 4),
            "peak_source": f"{peaks['source']} bf16 dense (burst)" +
                           ("; int8 runs as exact fp16 products on the same pipe" if dtype == "i8" else "")}
+    sustained = peaks.get("bf16_tflops_sustained")
+    if sustained:
+        # the measured rate of a seconds-long loop under the power cap, for
+        # context beside the burst figure the fraction is taken against
+        out["sustained_peak"] = float(sustained)
+        out["frac_of_sustained"] = round(achieved_tflops / float(sustained), 4)
     if dtype == "i8":
         # the integer MMA rate of this GPU, for context: the mma.sync engine's
         # 128 TOP/s on int8 4096^3 at 83 % integer-subpipe activity (ncu)

@@ -48,6 +48,10 @@ def test_roofline_fields():
     r = bench.roofline_for("bf16", 1800.0, 152, peaks)
     assert r["bound"] == "tensor" and r["peak"] == 1937.8
     assert r["frac"] == pytest.approx(1800.0 / 1937.8, abs=1e-4)
+    assert "frac_of_sustained" not in r  # only when a sustained figure was measured
+    r = bench.roofline_for("bf16", 1800.0, 152, {**peaks, "bf16_tflops_sustained": 1724.2})
+    assert r["frac"] == pytest.approx(1800.0 / 1937.8, abs=1e-4)
+    assert r["frac_of_sustained"] == pytest.approx(1800.0 / 1724.2, abs=1e-4)
     r = bench.roofline_for("i8", 1290.0, 152, peaks)
     assert r["unit"] == "TOP/s" and r["peak"] == 1937.8
     assert r["int8_mma_ceiling"]["ratio"] == pytest.approx(1290.0 / bench.INT8_MMA_CEILING_TOPS,
