@@ -75,6 +75,18 @@ def test_small_random(orc, dtype, M, N, K):
     check(orc, dtype, M, N, K, 1, 0, seed=1000 + M + N + K)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32", "i8"])
+@pytest.mark.parametrize("M,N,K", [
+    (1, 4097, 3000),     # one row; B's pitch odd (repacked / widened with padding)
+    (3000, 1, 4100),     # one column: C's pitch 1 element (no TMA store), K ragged
+    (1, 1, 65536),       # one output: its single tile cut along K by stream-K
+    (2, 8192, 512),
+    (8192, 2, 512),
+])
+def test_vector_like_shapes(orc, dtype, M, N, K):
+    check(orc, dtype, M, N, K, 1, 0, seed=3000 + M + N + K)
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (300, 520, 200), (257, 129, 1000)])
 def test_small_integer_valued_is_bit_exact(orc, dtype, M, N, K):
