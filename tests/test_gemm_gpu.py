@@ -114,6 +114,29 @@ def test_beta_zero_does_not_read_c(orc, dtype):
     compare(dtype, got, ref, A, B, K)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_beta_zero_does_not_read_c_on_stream_k_shapes(orc, dtype):
+    """The stream-K paths (bf16: pieces exchanging partial sums; fp32: the tail
+    grid reducing its pieces into C) must not read C either when beta = 0."""
+    M, N, K = 1000, 1000, 4100
+    A, B, _ = operands(dtype, M, N, K, 42)
+    C = np.full((M, N), np.nan, np.float32)
+    ref = orc.gemm(dtype, A, B, None, 1.0, 0.0)
+    got, status = run_gpu(dtype, A, B, C, 1.0, 0.0)
+    assert status == 0
+    compare(dtype, got, ref, A, B, K)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32", "i8"])
+def test_alpha_zero_beta_one_returns_c(orc, dtype):
+    M, N, K = 1000, 1000, 4100  # stream-K shapes: every path applies alpha and beta
+    A, B, C = operands(dtype, M, N, K, 43)
+    got, status = run_gpu(dtype, A, B, C, 0, 1)
+    assert status == 0
+    compare(dtype, got, orc.gemm(dtype, A, B, C, 0, 1), A, B, K, exact=True)
+    assert np.array_equal(got.view(np.uint32), np.asarray(C).view(np.uint32))
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32", "i8"])
 def test_k_zero(orc, dtype):
     M, N = 150, 260
