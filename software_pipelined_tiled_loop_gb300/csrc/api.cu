@@ -61,6 +61,11 @@ static pgemm_status device_setup(int *dev_out, DeviceState **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PGEMM_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return PGEMM_ERR_UNSUPPORTED_DEVICE;
+    // Make the device's primary context current in this host thread: the
+    // tensor-map encoder is a driver call and needs one, and a thread whose
+    // first CUDA work is this call (a worker thread of the caller) may not
+    // have one yet.
+    if (cudaSetDevice(dev) != cudaSuccess) return PGEMM_ERR_CUDA;
     DeviceState &d = g_dev[dev];
     if (!d.init) {
         d.init = true;
