@@ -3,12 +3,15 @@
 
 Default workload (one GPU): fp32 SGEMM M = N = K = 4096, row-major, A, B and
 the initial C uniform in [-1, 1) from a fixed seed, alpha = 1, beta = 0.5 --
-the FFMA path.  The bf16 8192^3 and int8 4096^3 workloads are measured in the
-same run and reported under "also".
+the FFMA path.  The bf16 8192^3 and int8 4096^3 workloads, and the bf16 K
+sweep (M = N = 4096, K in {32, 64, 128, 512, 2048, 16384}) with the ragged
+4095 x 4097 x 4100 shape, are measured in the same run and reported under
+"also", each with its own roofline and clock record.
 
 A step is one library call C <- alpha*A*B + beta*C on operands already
 resident in HBM.  Between timed steps L2 is flushed by writing a buffer larger
-than L2, and each step is timed with CUDA events on the launching stream;
+than L2 and reading it back (so that L2 holds only clean lines when the call
+starts), and each step is timed with CUDA events on the launching stream;
 the K timed steps are bracketed by a barrier and a device synchronise, and the
 reported time is the maximum over ranks.
 
@@ -51,6 +54,15 @@ WORKLOADS = {
     "igemm_i8_4096": ("i8", 4096, 4096, 4096, "i8_uniform", si.config_seed(3)),
     "gemm_bf16_8192": ("bf16", 8192, 8192, 8192, "bf16_normal", si.config_seed(4)),
 }
+# The bf16 K sweep and the ragged shape: short K (fewer K-tiles than stages)
+# is bound by writing C, long K by the tensor pipe.  Same seeds as the
+# parity tests of these shapes.
+K_SWEEP = (32, 64, 128, 512, 2048, 16384)
+for _k in K_SWEEP:
+    WORKLOADS[f"gemm_bf16_4096x4096_k{_k}"] = ("bf16", 4096, 4096, _k, "bf16_normal",
+                                               si.config_seed(5, _k % 251))
+WORKLOADS["gemm_bf16_ragged_4095x4097x4100"] = ("bf16", 4095, 4097, 4100, "bf16_normal",
+                                                si.config_seed(6))
 DEFAULT_WORKLOAD = "sgemm_fp32_4096"
 # The pages' own figure for a workload, where they print one (TFLOP/s): the
 # double-buffered SGEMM of "Double Buffering: Software Pipelining the K-Loop"
@@ -65,6 +77,16 @@ def vs_baseline(workload: str, value: float):
     fig = PAGE_FIGURES.get(workload)
     return None if fig is None else float(f"{value / fig[0]:.4g}")
 L2_FLUSH_BYTES = 512 << 20  # > 129 MB of L2
+
+
+def l2_flush(flush, i: int):
+    """Evict A, B and C from L2 between timed steps: write a buffer larger
+    than L2, then read it back whole.  The read leaves L2 holding clean lines
+    only; after the write alone it would be full of dirty lines, and the next
+    call would pay for writing them back to HBM as its own data came in (an
+    HBM-bound call most of all)."""
+    flush.fill_(float(i))
+    return flush.sum()
 
 
 # ------------------------------------------------------------------ peaks ---
@@ -85,6 +107,34 @@ def ffma_peak_tflops(sm_count: int, mhz: float) -> float:
 
 
 INT8_MMA_CEILING_TOPS = 153.5  # 128.0 TOP/s measured at 83.4 % integer-subpipe activity
+
+
+def algorithmic_bytes(dtype: str, M: int, N: int, K: int, beta) -> int:
+    """HBM bytes a call must move at least: A and B read once, C written once
+    (and read once when beta != 0)."""
+    eb = {"f32": 4, "bf16": 2, "i8": 1}[dtype]
+    return (M * K + K * N) * eb + M * N * 4 * (2 if beta != 0 else 1)
+
+
+def roofline_point(dtype: str, M: int, N: int, K: int, beta, ms: float, sm_count: int,
+                   peaks: dict) -> dict:
+    """Roofline of one call timed at `ms`: against the HBM copy rate when its
+    arithmetic intensity is below the ridge (peak FLOP/s over HBM bytes/s),
+    else against the compute peak of its dtype."""
+    flops = 2.0 * M * N * K
+    tflops = flops / (ms * 1e-3) / 1e12
+    nbytes = algorithmic_bytes(dtype, M, N, K, beta)
+    if dtype != "f32":
+        ridge = float(peaks["bf16_tflops"]) * 1e12 / (float(peaks["hbm_gbs"]) * 1e9)
+        if flops / nbytes < ridge:
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            peak = float(peaks["hbm_gbs"])
+            return {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                    "frac": round(gbs / peak, 4), "bytes": int(nbytes),
+                    "peak_source": f"{peaks['source']} HBM copy rate",
+                    "intensity_flop_per_byte": round(flops / nbytes, 1),
+                    "ridge_flop_per_byte": round(ridge, 1)}
+    return roofline_for(dtype, tflops, sm_count, peaks)
 
 
 def roofline_for(dtype: str, achieved_tflops: float, sm_count: int, peaks: dict) -> dict:
@@ -353,7 +403,7 @@ def run_gpu_workload(name: str, steps: int, warmup: int, dist_ctx, with_e2e: boo
     t_wall = time.perf_counter()
     host_ahead(torch, stream, steps)
     for i in range(steps):
-        flush.fill_(float(i))  # evict A, B, C from L2 between timed steps
+        l2_flush(flush, i)  # evict A, B, C from L2 between timed steps
         starts[i].record(stream)
         fn(M, N, K, alpha, dA, dB, beta, dC)
         ends[i].record(stream)
@@ -367,7 +417,7 @@ def run_gpu_workload(name: str, steps: int, warmup: int, dist_ctx, with_e2e: boo
         # window covers a second of this load
         while time.perf_counter() - t_wall < 1.0:
             for i in range(8):
-                flush.fill_(float(i))
+                l2_flush(flush, i)
                 fn(M, N, K, alpha, dA, dB, beta, dC)
             torch.cuda.synchronize()
         clk = clocks.stop()
@@ -448,7 +498,7 @@ def run_point(dtype, M, N, K, recipe, cfg, steps, warmup, seed=None):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(steps)]
     for i in range(steps):  # queued back to back: host work overlaps the GPU
-        flush.fill_(float(i))
+        l2_flush(flush, i)
         ev[i][0].record(stream)
         fn(M, N, K, alpha, dA, dB, beta, dC, config=cfg)
         ev[i][1].record(stream)
@@ -644,7 +694,8 @@ def main():
 
     dtype, M, N, K, recipe, seed = WORKLOADS[args.workload]
     config = {"workload": args.workload, "dtype": dtype, "M": M, "N": N, "K": K,
-              "recipe": recipe, "seed": seed, "l2": "flushed between timed steps (512 MiB write)"}
+              "recipe": recipe, "seed": seed, "l2": "flushed between timed steps (512 MiB written, then read back: "
+                    "L2 holds clean lines when each call starts)"}
 
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))
@@ -701,9 +752,11 @@ def main():
                                  clocks=ClockSampler(gpu_index))
             also[other] = {"value": round(r["tflops"], 2), "clocks": r["clocks"],
                            "unit": "TOP/s" if r["dtype"] == "i8" else "TFLOP/s",
+                           "shape": [r["M"], r["N"], r["K"]],
                            "ms_per_step": round(r["ms_per_step"], 4),
                            "ms_median": round(r["ms_median"], 4),
-                           "roofline": roofline_for(r["dtype"], r["per_gpu_tflops"], sm_count, peaks),
+                           "roofline": roofline_point(r["dtype"], r["M"], r["N"], r["K"], r["beta"],
+                                                      r["ms_per_step"], sm_count, peaks),
                            "config": r["config"]}
 
     cpu = None

@@ -32,6 +32,7 @@ constexpr int kMaxDevices = 64;
 struct KernelState {
     bool ready = false;
     int blocks_per_sm = 0;
+    int slots = 0;  // schedule slots of a persistent launch (0: not persistent)
 };
 
 struct DeviceState {
@@ -47,6 +48,11 @@ struct DeviceState {
     std::unordered_map<const void *, KernelState> kernels;
 };
 
+// Guards the one-time set-up of a device and of each kernel on it (and the
+// table of kernels already set up).  Everything after that set-up -- the
+// choice of configuration, scratch allocation, tensor-map encoding and the
+// launches -- runs without it, so host threads calling on their own streams
+// enqueue concurrently.
 static std::mutex g_mu;
 static DeviceState g_dev[kMaxDevices];
 
@@ -108,7 +114,11 @@ static pgemm_status device_setup(int *dev_out, DeviceState **out) {
     return d.init_status;
 }
 
-static pgemm_status kernel_setup(DeviceState &d, const KernelInfo &k, int *blocks_per_sm) {
+// One-time set-up of a kernel on a device (under g_mu): shared-memory
+// attributes, resident blocks per SM and, for the persistent kernels, the
+// number of schedule slots of a launch.
+static pgemm_status kernel_setup(DeviceState &d, const KernelInfo &k, int *blocks_per_sm,
+                                 int *slots = nullptr) {
     KernelState &ks = d.kernels[k.func];
     if (!ks.ready) {
         if (cudaFuncSetAttribute(k.func, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -130,10 +140,17 @@ static pgemm_status kernel_setup(DeviceState &d, const KernelInfo &k, int *block
             cudaSuccess)
             return PGEMM_ERR_CUDA;
         if (n < 1) return PGEMM_ERR_UNSUPPORTED_CONFIG;
+        if (k.schedule_slots != nullptr) {
+            LaunchCommon q{};
+            q.sm_count = d.sm_count;
+            q.blocks_per_sm = n;
+            if (k.schedule_slots(q, &ks.slots) != cudaSuccess) return PGEMM_ERR_CUDA;
+        }
         ks.blocks_per_sm = n;
         ks.ready = true;
     }
     *blocks_per_sm = ks.blocks_per_sm;
+    if (slots) *slots = ks.slots;
     return PGEMM_OK;
 }
 
@@ -311,47 +328,47 @@ struct Scratch {
 
 enum class Kind { F32, BF16, I8 };
 
-// fixed_scratch: when given, operand repacking / widening uses this device
-// buffer of fixed_scratch_bytes instead of stream-ordered allocations, and a
-// problem that does not fit is rejected with PGEMM_ERR_TOO_LARGE.
+// fixed_scratch (FixedScratchFn, kernels.h): when given, operand repacking / widening uses the buffer it
+// provides instead of stream-ordered allocations, a problem that does not
+// fit is rejected with PGEMM_ERR_TOO_LARGE, and no tile is split (the
+// stream-K exchange would need memory too).
 template <Kind KIND, typename In, typename Sc, typename Out>
 static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const In *B, Sc beta,
                               Out *C, const pgemm_config *cfg_in, cudaStream_t stream,
-                              void *fixed_scratch = nullptr, long long fixed_scratch_bytes = 0) {
+                              FixedScratchFn fixed_scratch = nullptr) {
     if (M < 0 || N < 0 || K < 0) return PGEMM_ERR_INVALID_VALUE;
     if (M == 0 || N == 0) return PGEMM_OK;
     if (C == nullptr || (K > 0 && (A == nullptr || B == nullptr))) return PGEMM_ERR_INVALID_VALUE;
     if (!aligned16(C) || (K > 0 && (!aligned16(A) || !aligned16(B)))) return PGEMM_ERR_MISALIGNED;
+    if (cfg_in && cfg_in->max_k_parts < 0) return PGEMM_ERR_INVALID_VALUE;
     constexpr pgemm_dtype DT =
         KIND == Kind::F32 ? PGEMM_F32 : (KIND == Kind::BF16 ? PGEMM_BF16 : PGEMM_I8);
 
-    std::lock_guard<std::mutex> lock(g_mu);
     int dev = 0;
     DeviceState *d = nullptr;
-    pgemm_status st = device_setup(&dev, &d);
-    if (st != PGEMM_OK) return st;
-
-    pgemm_config c = (cfg_in && cfg_in->stages > 0) ? *cfg_in : default_config(DT, M, N, K, d->sm_count);
-    if (c.bm == 0) c.bm = 128;
-    if (cfg_in) c.max_k_parts = cfg_in->max_k_parts;
-    if (c.max_k_parts < 0) return PGEMM_ERR_INVALID_VALUE;
-    const KernelInfo *k = find_kernel(DT, c);
-    if (!k) return PGEMM_ERR_UNSUPPORTED_CONFIG;
-    int blocks_per_sm = 0;
-    st = kernel_setup(*d, *k, &blocks_per_sm);
-    if (st != PGEMM_OK) return st;
+    pgemm_config c{};
+    const KernelInfo *k = nullptr;
+    int blocks_per_sm = 0, slots = 0;
+    {
+        // one-time set-up only; the rest of the call runs unlocked
+        std::lock_guard<std::mutex> lock(g_mu);
+        pgemm_status st = device_setup(&dev, &d);
+        if (st != PGEMM_OK) return st;
+        c = (cfg_in && cfg_in->stages > 0) ? *cfg_in : default_config(DT, M, N, K, d->sm_count);
+        if (c.bm == 0) c.bm = 128;
+        if (cfg_in) c.max_k_parts = cfg_in->max_k_parts;
+        k = find_kernel(DT, c);
+        if (!k) return PGEMM_ERR_UNSUPPORTED_CONFIG;
+        st = kernel_setup(*d, *k, &blocks_per_sm, &slots);
+        if (st != PGEMM_OK) return st;
+    }
+    pgemm_status st = PGEMM_OK;
 
     // The persistent schedule (tensor-core kernels).  A call with a fixed
     // scratch buffer does not split: the exchange area would need memory.
     TileSchedule sched;
-    if (k->schedule_slots != nullptr) {
-        LaunchCommon q{};
-        q.sm_count = d->sm_count;
-        q.blocks_per_sm = blocks_per_sm;
-        int slots = 0;
-        if (k->schedule_slots(q, &slots) != cudaSuccess) return PGEMM_ERR_CUDA;
+    if (k->schedule_slots != nullptr)
         sched = plan_schedule(*k, M, N, K, slots, fixed_scratch != nullptr ? 1 : c.max_k_parts);
-    }
 
     // Operands as the kernels read them: element type, pitch, base pointer.
     // int8 is widened to fp16 by a pre-pass, except for the mma.sync engine,
@@ -398,8 +415,12 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
             const long long b_bytes = b_repack ? round_up(b_ld2 * b_rows * in_bytes, 256) : 0;
             uint8_t *base = nullptr;
             if (fixed_scratch != nullptr) {
-                if (a_bytes + b_bytes > fixed_scratch_bytes) return PGEMM_ERR_TOO_LARGE;
-                base = static_cast<uint8_t *>(fixed_scratch);
+                void *fp = nullptr;
+                long long fbytes = 0;
+                st = fixed_scratch(&fp, &fbytes);
+                if (st != PGEMM_OK) return st;
+                if (a_bytes + b_bytes > fbytes) return PGEMM_ERR_TOO_LARGE;
+                base = static_cast<uint8_t *>(fp);
             } else {
                 if (cudaMallocFromPoolAsync(&scratch.p, a_bytes + b_bytes, d->pool, stream) !=
                     cudaSuccess)
@@ -531,13 +552,13 @@ __global__ void selftest_wait_kernel(KernelCtx ctx) {
     if (threadIdx.x == 0) mbar_wait(&bar, 0, ctx, kSiteSelfTest);
 }
 
-// The int8 GEMM with its widened operands placed in a caller-supplied device
-// buffer (no allocation); used by the no-allocation entry point.
+// The int8 GEMM with its widened operands placed in the fixed device buffer
+// that `scratch` provides (no allocation); used by the no-allocation entry
+// point.
 pgemm_status gemm_i8_fixed_scratch(int M, int N, int K, int32_t alpha, const int8_t *A,
-                                   const int8_t *B, int32_t beta, int32_t *C, void *scratch,
-                                   long long scratch_bytes, cudaStream_t stream) {
-    return gemm_impl<Kind::I8>(M, N, K, alpha, A, B, beta, C, nullptr, stream, scratch,
-                               scratch_bytes);
+                                   const int8_t *B, int32_t beta, int32_t *C,
+                                   FixedScratchFn scratch, cudaStream_t stream) {
+    return gemm_impl<Kind::I8>(M, N, K, alpha, A, B, beta, C, nullptr, stream, scratch);
 }
 
 }  // namespace pg
@@ -689,16 +710,11 @@ pgemm_status pgemm_schedule(pgemm_dtype dtype, const pgemm_config *cfg, int M, i
     if (c.max_k_parts < 0) return PGEMM_ERR_INVALID_VALUE;
     const KernelInfo *k = find_kernel(dtype, c);
     if (!k) return PGEMM_ERR_UNSUPPORTED_CONFIG;
-    int bps = 0;
-    st = kernel_setup(*d, *k, &bps);
+    int bps = 0, n = 0;
+    st = kernel_setup(*d, *k, &bps, &n);
     if (st != PGEMM_OK) return st;
     TileSchedule s;
     if (k->schedule_slots != nullptr) {
-        LaunchCommon q{};
-        q.sm_count = d->sm_count;
-        q.blocks_per_sm = bps;
-        int n = 0;
-        if (k->schedule_slots(q, &n) != cudaSuccess) return PGEMM_ERR_CUDA;
         s = plan_schedule(*k, M, N, K, n, c.max_k_parts);
     } else {
         s.tiles = static_cast<long long>((M + k->bm - 1) / k->bm) * ((N + k->bn - 1) / k->bn);

@@ -24,19 +24,24 @@ void *g_scratch_addr[kMaxDevices] = {};
 
 // Device address of the array on the current device, looked up once per
 // device.  In host code the array's name stands for a host-side shadow, not
-// for device memory, so the kernels are given this address instead.
-pgemm_status scratch_address(void **out) {
+// for device memory, so the kernels are given this address instead.  The
+// GEMM calls this only after it has checked the arguments and set up the
+// device (an sm_103 device is current), and only when it needs the array.
+pgemm_status scratch_address(void **out, long long *bytes) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PGEMM_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return PGEMM_ERR_UNSUPPORTED_DEVICE;
     std::lock_guard<std::mutex> lock(g_setup_mu);
     if (g_scratch_addr[dev] == nullptr) {
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+            cudaGetLastError();  // leave no error behind for the caller's next check
             return PGEMM_ERR_CUDA;
+        }
         g_scratch_addr[dev] = p;
     }
     *out = g_scratch_addr[dev];
+    *bytes = static_cast<long long>(PGEMM_NOALLOC_SCRATCH_BYTES);
     return PGEMM_OK;
 }
 
@@ -45,11 +50,5 @@ pgemm_status scratch_address(void **out) {
 extern "C" pgemm_status gemm_i8_noalloc(int M, int N, int K, int32_t alpha, const int8_t *A,
                                         const int8_t *B, int32_t beta, int32_t *C,
                                         pgemm_stream_t stream) {
-    if (M < 0 || N < 0 || K < 0) return PGEMM_ERR_INVALID_VALUE;
-    if (M == 0 || N == 0) return PGEMM_OK;
-    void *scratch = nullptr;
-    const pgemm_status st = scratch_address(&scratch);
-    if (st != PGEMM_OK) return st;
-    return pg::gemm_i8_fixed_scratch(M, N, K, alpha, A, B, beta, C, scratch,
-                                     static_cast<long long>(PGEMM_NOALLOC_SCRATCH_BYTES), stream);
+    return pg::gemm_i8_fixed_scratch(M, N, K, alpha, A, B, beta, C, scratch_address, stream);
 }

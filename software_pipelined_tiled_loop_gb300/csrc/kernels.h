@@ -127,11 +127,15 @@ cudaError_t launch_i8_relayout(const int8_t *src, long long sld, void *dst, long
 }  // namespace pg
 
 namespace pg {
-// api.cu: the int8 GEMM using `scratch` (scratch_bytes long) for its widened
-// operands instead of allocating; PGEMM_ERR_TOO_LARGE if they do not fit.
+// api.cu: the int8 GEMM using a fixed device buffer for its widened operands
+// instead of allocating; PGEMM_ERR_TOO_LARGE if they do not fit.  `scratch`
+// gives the buffer's address and size on the current device; it is called
+// after the arguments are checked and the device is set up, and only when
+// the call needs scratch.
+using FixedScratchFn = pgemm_status (*)(void **ptr, long long *bytes);
 pgemm_status gemm_i8_fixed_scratch(int M, int N, int K, int32_t alpha, const int8_t *A,
-                                   const int8_t *B, int32_t beta, int32_t *C, void *scratch,
-                                   long long scratch_bytes, cudaStream_t stream);
+                                   const int8_t *B, int32_t beta, int32_t *C,
+                                   FixedScratchFn scratch, cudaStream_t stream);
 }  // namespace pg
 
 namespace pg {

@@ -74,10 +74,11 @@ def test_list_configs(L):
     assert not [c for c in f32 + bf16 if len(c) > 6 and c[6] != pg.ENGINES["default"]]
 
 
-@pytest.mark.parametrize("fn", ["gemm_f32", "gemm_bf16", "gemm_i8"])
+@pytest.mark.parametrize("fn", ["gemm_f32", "gemm_bf16", "gemm_i8", "gemm_i8_noalloc"])
 def test_host_validation_without_gpu(L, fn):
+    # gemm_i8_noalloc checks its arguments before it looks up its device array
     f = getattr(L, fn)
-    a = 1 if fn == "gemm_i8" else 1.0
+    a = 1 if fn.startswith("gemm_i8") else 1.0
     good = 1 << 20  # never dereferenced: validation fails or the call is a no-op first
     # negative dimensions
     assert f(-1, 4, 4, a, good, good, 0 * a, good, None) == 1

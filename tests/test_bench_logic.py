@@ -95,3 +95,33 @@ def test_vs_baseline_uses_the_pages_figure_only_where_they_print_one():
     assert bench.vs_baseline("sgemm_fp32_4096", 64.215) == pytest.approx(2.0, abs=1e-3)
     assert bench.vs_baseline("gemm_bf16_8192", 1800.0) is None
     assert bench.vs_baseline("igemm_i8_4096", 1280.0) is None
+
+
+def test_k_sweep_and_ragged_are_bench_workloads():
+    # the bf16 K sweep (M = N = 4096) and the ragged shape run beside the
+    # headline, with the parity tests' seeds
+    import seeded_inputs as si
+    for k in (32, 64, 128, 512, 2048, 16384):
+        w = bench.WORKLOADS[f"gemm_bf16_4096x4096_k{k}"]
+        assert w[:4] == ("bf16", 4096, 4096, k) and w[5] == si.config_seed(5, k % 251)
+    assert bench.WORKLOADS["gemm_bf16_ragged_4095x4097x4100"][:4] == ("bf16", 4095, 4097, 4100)
+
+
+def test_roofline_point_picks_the_bound_by_intensity():
+    peaks = {"bf16_tflops": 1937.8, "hbm_gbs": 6791.4, "sm_max_mhz": 2070.0, "source": "measured"}
+    M = N = 4096
+    # K <= 512: below the ridge (1937.8e12 / 6791.4e9 = 285 FLOP/B): HBM-bound,
+    # bytes = C written once (fp32, beta = 0) + bf16 A and B read once
+    for K in (32, 64, 128, 512):
+        r = bench.roofline_point("bf16", M, N, K, 0.0, 0.02, 152, peaks)
+        nbytes = 4 * M * N + 2 * K * (M + N)
+        assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["bytes"] == nbytes
+        assert r["achieved"] == pytest.approx(nbytes / 0.02e-3 / 1e9, rel=1e-3)
+        assert r["frac"] == pytest.approx(r["achieved"] / 6791.4, abs=1e-4)
+    for K in (2048, 16384):
+        r = bench.roofline_point("bf16", M, N, K, 0.0, 0.05, 152, peaks)
+        assert r["bound"] == "tensor"
+        assert r["achieved"] == pytest.approx(2.0 * M * N * K / 0.05e-3 / 1e12, rel=1e-3)
+    # beta != 0 reads C as well; fp32 is always against the FFMA peak
+    assert bench.algorithmic_bytes("f32", 4096, 4096, 4096, 0.5) == 4 * (2 * 4096 ** 2 + 2 * 4096 ** 2)
+    assert bench.roofline_point("f32", 4096, 4096, 4096, 0.5, 2.1, 152, peaks)["bound"] == "alu"
