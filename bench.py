@@ -514,7 +514,8 @@ def run_point(dtype, M, N, K, recipe, cfg, steps, warmup, seed=None):
     del dA, dB, dC, flush
     return {"dtype": dtype, "M": M, "N": N, "K": K, "bm": cfg[0], "bn": cfg[1], "bk": cfg[2],
             "stages": cfg[3], "max_k_parts": cfg[4] if len(cfg) > 4 else 0,
-            "producer": {0: "tma", 1: "registers"}[cfg[5] if len(cfg) > 5 else 0],
+            "group_m": cfg[7] if len(cfg) > 7 else 0,
+            "producer": {0: "tma", 1: "registers", 2: "staged"}[cfg[5] if len(cfg) > 5 else 0],
             "k_tiles": -(-K // cfg[2]), **attrs, **sched, "ms_median": round(med, 4),
             "ms_min": round(min(ms), 4), "tflops": round(flops / (med * 1e-3) / 1e12, 2),
             "gbs": round((in_bytes + out_bytes) / (med * 1e-3) / 1e9, 1), "status": status}
@@ -667,7 +668,7 @@ def main():
     ap.add_argument("--hazard", type=int, default=0,
                     help="run the stage-reuse hazard experiment this many iterations per variant")
     ap.add_argument("--point", default=None,
-                    help="dtype,M,N,K,bm,bn,bk,stages[,max_k_parts[,producer[,engine]]]: time one point "
+                    help="dtype,M,N,K,bm,bn,bk,stages[,max_k_parts[,producer[,engine[,group_m]]]]: time one point "
                          "(for profiler captures and split / no-split comparisons)")
     args = ap.parse_args()
     if args.warmup < 3:

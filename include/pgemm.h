@@ -96,8 +96,19 @@ typedef enum { PGEMM_F32 = 0, PGEMM_BF16 = 1, PGEMM_I8 = 2 } pgemm_dtype;
  *       load the int8 tiles, widen them exactly to fp16 in registers and
  *       store them into the S-stage ring the tensor core reads, so no
  *       widening pass runs; the MMA issuer and the exact-round epilogue are
- *       the default kernel's. */
-typedef enum { PGEMM_PRODUCER_TMA = 0, PGEMM_PRODUCER_REGISTERS = 1 } pgemm_producer;
+ *       the default kernel's.
+ *   PGEMM_PRODUCER_STAGED (int8, CTA pair 256 x 256): TMA copies the int8
+ *     tiles as they are into a ring of `stages` int8 stages (16 KB each per
+ *     CTA, half an fp16 stage), and four warps per CTA widen each landed
+ *     stage exactly to fp16 into a short ring of fp16 stages that the tensor
+ *     core reads (shared memory to shared memory).  No widening pass runs and
+ *     the operands cross L2 as int8; the MMA issuer and the exact-round
+ *     epilogue are the default kernel's. */
+typedef enum {
+    PGEMM_PRODUCER_TMA = 0,
+    PGEMM_PRODUCER_REGISTERS = 1,
+    PGEMM_PRODUCER_STAGED = 2
+} pgemm_producer;
 
 /* Which multiply-accumulate consumes the stages (pgemm_config.engine).
  *   PGEMM_ENGINE_DEFAULT: FFMA register tiles (fp32), tcgen05.mma into
@@ -125,11 +136,18 @@ typedef enum { PGEMM_ENGINE_DEFAULT = 0, PGEMM_ENGINE_MMA_SYNC = 1 } pgemm_engin
  * the alpha/beta update.  max_k_parts = 0: the library's choice (at most 2
  * pieces a tile for the tensor-core kernels, whose exchange is slower than
  * the fp32 kernels'; none for fp32); 1: off; n > 1: at most n pieces a tile. */
+/* group_m (the pages have no counterpart): the order in which output tiles
+ * are handed out.  Tiles go down group_m tile rows (tile pairs for a CTA
+ * pair), then one tile column to the right, and so on across C, then the
+ * next group of rows: the CTAs running at once share A row panels and B
+ * column panels through L2, and group_m sets the shape of that working set.
+ * 0: the library's choice (16 for the tensor-core kernels, 8 otherwise). */
 typedef struct {
     int bm, bn, bk, stages;
     int max_k_parts;
     int producer; /* a pgemm_producer */
     int engine;   /* a pgemm_engine */
+    int group_m;  /* raster group of the tile order (0: the library's choice) */
 } pgemm_config;
 
 /* fp32: FFMA register-tiled consumers on the pipelined ring.  Semantics are

@@ -36,7 +36,7 @@ STATUS = {
 NOALLOC_SCRATCH_BYTES = 32 << 20
 DTYPES = {"f32": 0, "bf16": 1, "i8": 2}
 # pgemm_producer: who fills the shared-memory stages
-PRODUCERS = {"tma": 0, "registers": 1}
+PRODUCERS = {"tma": 0, "registers": 1, "staged": 2}
 # pgemm_engine: which multiply-accumulate consumes the stages
 ENGINES = {"default": 0, "mma_sync": 1}
 # Every function include/pgemm.h declares.
@@ -59,15 +59,18 @@ class PgemmError(RuntimeError):
 
 class Config(ctypes.Structure):
     """pgemm_config.  A tuple (bm, bn, bk, stages[, max_k_parts[, producer[,
-    engine]]]) converts to it."""
+    engine[, group_m]]]]) converts to it."""
     _fields_ = [("bm", ctypes.c_int), ("bn", ctypes.c_int), ("bk", ctypes.c_int),
                 ("stages", ctypes.c_int), ("max_k_parts", ctypes.c_int),
-                ("producer", ctypes.c_int), ("engine", ctypes.c_int)]
+                ("producer", ctypes.c_int), ("engine", ctypes.c_int), ("group_m", ctypes.c_int)]
 
     def as_tuple(self):
         """The kernel the configuration names: (bm, bn, bk, stages), with
         (..., max_k_parts, producer, engine) appended when the producer or
-        the engine is not the default."""
+        the engine is not the default, and group_m after them when set."""
+        if self.group_m:
+            return (self.bm, self.bn, self.bk, self.stages, self.max_k_parts, self.producer,
+                    self.engine, self.group_m)
         if self.producer or self.engine:
             return (self.bm, self.bn, self.bk, self.stages, self.max_k_parts, self.producer,
                     self.engine)

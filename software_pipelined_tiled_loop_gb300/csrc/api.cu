@@ -340,7 +340,7 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
     if (M == 0 || N == 0) return PGEMM_OK;
     if (C == nullptr || (K > 0 && (A == nullptr || B == nullptr))) return PGEMM_ERR_INVALID_VALUE;
     if (!aligned16(C) || (K > 0 && (!aligned16(A) || !aligned16(B)))) return PGEMM_ERR_MISALIGNED;
-    if (cfg_in && cfg_in->max_k_parts < 0) return PGEMM_ERR_INVALID_VALUE;
+    if (cfg_in && (cfg_in->max_k_parts < 0 || cfg_in->group_m < 0)) return PGEMM_ERR_INVALID_VALUE;
     constexpr pgemm_dtype DT =
         KIND == Kind::F32 ? PGEMM_F32 : (KIND == Kind::BF16 ? PGEMM_BF16 : PGEMM_I8);
 
@@ -356,7 +356,10 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
         if (st != PGEMM_OK) return st;
         c = (cfg_in && cfg_in->stages > 0) ? *cfg_in : default_config(DT, M, N, K, d->sm_count);
         if (c.bm == 0) c.bm = 128;
-        if (cfg_in) c.max_k_parts = cfg_in->max_k_parts;
+        if (cfg_in) {
+            c.max_k_parts = cfg_in->max_k_parts;
+            if (cfg_in->group_m > 0) c.group_m = cfg_in->group_m;
+        }
         k = find_kernel(DT, c);
         if (!k) return PGEMM_ERR_UNSUPPORTED_CONFIG;
         st = kernel_setup(*d, *k, &blocks_per_sm, &slots);
@@ -373,11 +376,14 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
     // Operands as the kernels read them: element type, pitch, base pointer.
     // int8 is widened to fp16 by a pre-pass, except for the mma.sync engine,
     // which reads the int8 values with B transposed (N rows of K), and the
-    // register-staged producer, which reads them as they are (rows relaid
-    // out to 16-byte pitches when K or N is not a multiple of 16).
+    // register-staged and staged producers, which read them as they are
+    // (rows relaid out to 16-byte pitches when K or N is not a multiple of 16).
     const bool imma = KIND == Kind::I8 && k->engine == PGEMM_ENGINE_MMA_SYNC;
     const bool rp = KIND == Kind::I8 && !imma && k->producer == PGEMM_PRODUCER_REGISTERS;
-    const int in_bytes = KIND == Kind::F32 ? 4 : ((imma || rp) ? 1 : 2);
+    // the staged producer's TMA copies the int8 operands as they are
+    const bool staged = KIND == Kind::I8 && !imma && k->producer == PGEMM_PRODUCER_STAGED;
+    const bool raw_i8 = rp || staged;  // the kernel reads int8 (no widening pass)
+    const int in_bytes = KIND == Kind::F32 ? 4 : ((imma || raw_i8) ? 1 : 2);
     const long long lda = K, ldb = N;
     const void *a_op = A;
     const void *b_op = B;
@@ -396,14 +402,14 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
         // The counters start at zero: the int8 widening pass (which the GEMM
         // waits for) zeroes them; otherwise a memset before any pre-pass does,
         // so that a programmatic launch after the pre-pass still finds them zero.
-        if (!(KIND == Kind::I8 && k->engine == PGEMM_ENGINE_DEFAULT && !rp && K > 0) &&
+        if (!(KIND == Kind::I8 && k->engine == PGEMM_ENGINE_DEFAULT && !raw_i8 && K > 0) &&
             cudaMemsetAsync(sched.counters, 0, cbytes, stream) != cudaSuccess)
             return PGEMM_ERR_CUDA;
     }
     std::function<cudaError_t()> prepass;  // repack / widening launch, if any
     if (K > 0) {
         const long long align_elems = 16 / in_bytes;
-        const bool widen = KIND == Kind::I8 && !imma && !rp;
+        const bool widen = KIND == Kind::I8 && !imma && !raw_i8;
         const bool a_repack = widen || (lda * in_bytes) % 16 != 0;
         const bool b_repack = widen || imma || (ldb * in_bytes) % 16 != 0;
         if (a_repack || b_repack) {
@@ -430,7 +436,7 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
             // The pre-pass is launched below, after every tensor map is encoded,
             // so that the GEMM launch follows it with no host work in between.
             prepass = [=, &d]() -> cudaError_t {
-                if (imma || rp) {  // int8 to 16-byte pitches as needed; mma.sync: B -> B^T
+                if (imma || raw_i8) {  // int8 to 16-byte pitches as needed; mma.sync: B -> B^T
                     cudaError_t e = cudaSuccess;
                     if (a_repack)
                         e = launch_i8_relayout(reinterpret_cast<const int8_t *>(A), lda, base,
@@ -473,7 +479,7 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
     alignas(64) CUtensorMap ta, tb;
     const CUtensorMapDataType tmt = KIND == Kind::F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                     : KIND == Kind::BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                    : (imma || rp)       ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                    : (imma || raw_i8)   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     if (K > 0 && imma) {
         st = encode_2d(&ta, tmt, 1, a_op, K, M, a_ld, k->a_box_x, k->a_box_y, k->a_swizzle128);
@@ -509,7 +515,7 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
     KernelCtx ctx{d->status, kDefaultWaitLimitNs};
     if constexpr (KIND == Kind::F32) {
         LaunchF32 p{};
-        p.M = M; p.N = N; p.K = K; p.ldc = N; p.group_m = 0;
+        p.M = M; p.N = N; p.K = K; p.ldc = N; p.group_m = c.group_m;
         p.sm_count = d->sm_count; p.blocks_per_sm = blocks_per_sm;
         p.tmap_a = &ta; p.tmap_b = &tb; p.tmap_c = tmap_c; p.ctx = ctx;
         p.a_ptr = a_op; p.b_ptr = b_op; p.lda = a_ld; p.ldb = b_ld;
@@ -519,7 +525,7 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
         e = k->launch_f32(p, stream);
     } else if constexpr (KIND == Kind::BF16) {
         LaunchBf16 p{};
-        p.M = M; p.N = N; p.K = K; p.ldc = N; p.group_m = 0;
+        p.M = M; p.N = N; p.K = K; p.ldc = N; p.group_m = c.group_m;
         p.sm_count = d->sm_count; p.blocks_per_sm = blocks_per_sm;
         p.tmap_a = &ta; p.tmap_b = &tb; p.tmap_c = tmap_c; p.ctx = ctx;
         p.a_ptr = a_op; p.b_ptr = b_op; p.lda = a_ld; p.ldb = b_ld;
@@ -529,7 +535,7 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
         e = k->launch_bf16(p, stream);
     } else {
         LaunchI8 p{};
-        p.M = M; p.N = N; p.K = K; p.ldc = N; p.group_m = 0;
+        p.M = M; p.N = N; p.K = K; p.ldc = N; p.group_m = c.group_m;
         p.sm_count = d->sm_count; p.blocks_per_sm = blocks_per_sm;
         p.tmap_a = &ta; p.tmap_b = &tb; p.tmap_c = tmap_c; p.ctx = ctx;
         p.a_ptr = a_op; p.b_ptr = b_op; p.lda = a_ld; p.ldb = b_ld;
@@ -614,7 +620,7 @@ pgemm_status pgemm_default_config(pgemm_dtype dtype, int M, int N, int K, pgemm_
 int pgemm_list_configs(pgemm_dtype dtype, pgemm_config *out, int cap) {
     int n = 0;
     const KernelInfo *t = table_of(dtype, &n);
-    for (int i = 0; i < n && i < cap && out; ++i) out[i] = pgemm_config{t[i].bm, t[i].bn, t[i].bk, t[i].stages, 0, t[i].producer, t[i].engine};
+    for (int i = 0; i < n && i < cap && out; ++i) out[i] = pgemm_config{t[i].bm, t[i].bn, t[i].bk, t[i].stages, 0, t[i].producer, t[i].engine, 0};
     return n;
 }
 

@@ -29,14 +29,25 @@ constexpr int kI8ChunkTiles = 16;  // 16 K-tiles of 64 = 1024 products per exact
 
 // Each epilogue thread keeps a 128-column row of int32 sums in registers:
 // 128-wide tiles use four epilogue warps, 256-wide tiles eight.
-template <int BN, int STAGES, int CM = 1, int PROD = 0>
+template <int BN, int STAGES, int CM = 1, int PROD = 0, int S8 = 0, int XG = 1>
 using I8Cfg = TcCfg<BN, STAGES, kI8ChunkTiles, /*BF16=*/0, /*INT_FOLD=*/true, BN == 256 ? 8 : 4,
-                    CM, CM, PROD>;
+                    CM, CM, PROD, S8, XG>;
 
-template <int BN, int STAGES, int CM = 1, int PROD = 0>
+template <int BN, int STAGES, int CM = 1, int PROD = 0, int S8 = 0, int XG = 1>
 static KernelInfo info_i8() {
-    KernelInfo k = tc_info<I8Cfg<BN, STAGES, CM, PROD>>();
-    k.launch_i8 = launch_tc<I8Cfg<BN, STAGES, CM, PROD>, LaunchI8>;
+    using Cfg = I8Cfg<BN, STAGES, CM, PROD, S8, XG>;
+    KernelInfo k = tc_info<Cfg>();
+    k.launch_i8 = launch_tc<Cfg, LaunchI8>;
+    return k;
+}
+
+// The staged producer on the CTA pair: `stages` names the depth of the int8
+// ring (the one that covers the memory latency); the fp16 ring behind it is
+// F16 deep (it only covers the widening); two transform groups.
+template <int S8, int F16>
+static KernelInfo info_i8_staged() {
+    KernelInfo k = info_i8<256, F16, 2, 2, S8, 2>();
+    k.stages = S8;
     return k;
 }
 
@@ -50,6 +61,8 @@ const KernelInfo *i8_kernels(int *count) {
             info_i8<256, 4, 2>(), info_i8<256, 5, 2>(), info_i8<256, 6, 2>(),
             // CTA pair with the register-staged producer (int8 read directly)
             info_i8<256, 4, 2, 1>(), info_i8<256, 5, 2, 1>(), info_i8<256, 6, 2, 1>(),
+            // CTA pair with int8 stages by TMA, widened in shared memory
+            info_i8_staged<4, 3>(), info_i8_staged<5, 3>(), info_i8_staged<6, 2>(),
         };
         int n = 0;
         const KernelInfo *imma = i8_imma_kernels(&n);

@@ -74,8 +74,14 @@ namespace pg {
 // epilogue warps are 4 .. 4 + EPI - 1 and the MMA issuer is warp 4 + EPI,
 // and every role is a whole warpgroup, so that setmaxnreg can move
 // registers from the producers and the MMA warpgroup to the epilogue.
+// 2: the int8 tiles arrive by TMA in a second ring of S8 int8 stages (half
+// the bytes of an fp16 stage), filled by one lane of warp 4 + EPI + 1; the
+// four warps 0-3 widen each landed int8 stage into the fp16 stage the tensor
+// core reads (shared memory to shared memory) in XG groups that take
+// alternate K-tiles.  No widening pass, and the int8 operands cross L2 once
+// at half the fp16 bytes.
 template <int BN_, int STAGES_, int KC_, int BF16_, bool INT_FOLD_, int EPI_ = 4, int CM_ = 1,
-          int CG_ = 1, int PROD_ = 0>
+          int CG_ = 1, int PROD_ = 0, int S8_ = 0, int XG_ = 1>
 struct TcCfg {
     static constexpr int BM = 128, BN = BN_, BK = 64, STAGES = STAGES_, KC = KC_, CM = CM_;
     static constexpr int CG = CG_;
@@ -89,25 +95,38 @@ struct TcCfg {
     static constexpr int B_BYTES = B_COLS * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // per CTA
     static constexpr int TX_BYTES = STAGE_BYTES * CG;      // counted on the MMA's full barrier
+    // PROD = 2: the int8 staging ring (A 128 x 64 bytes, then B as B_COLS/64
+    // boxes of 64 k-rows x 64 bytes; 64-byte rows, unswizzled).
+    static constexpr int S8 = PROD_ == 2 ? S8_ : 0;
+    static constexpr int XG = PROD_ == 2 ? XG_ : 1;        // transform groups
+    static constexpr int XG_WARPS = 4 / XG;                // warps per transform group
+    static constexpr int A8_BYTES = BM * BK;               // int8
+    static constexpr int STAGE8_BYTES = (BM + B_COLS) * BK;
+    static constexpr int RING8_BYTES = S8 * STAGE8_BYTES;
     // Epilogue staging: one or two 32x32 fp32 blocks per epilogue warp (two
     // let a TMA store drain while the next block is staged), as many as fit.
-    static constexpr int STAGE_BUFS =
-        STAGES * STAGE_BYTES + EPI * 2 * 4096 + (2 * STAGES + 5) * 8 + 16 + 1024 <= 232448 ? 2 : 1;
+    static constexpr int STAGE_BUFS = STAGES * STAGE_BYTES + RING8_BYTES + EPI * 2 * 4096 +
+                                                  (2 * STAGES + 5 + 2 * S8) * 8 + 16 + 1024 <=
+                                              232448
+                                          ? 2
+                                          : 1;
     static constexpr int STAGING_BYTES = EPI * STAGE_BUFS * 32 * 32 * 4;
     static constexpr int ACC_COLS = BN;        // fp32 accumulator: one TMEM column per n
     static constexpr int TMEM_COLS = 2 * BN;   // two accumulators
     static constexpr int PROD = PROD_;
     static constexpr int EPI_WARP0 = PROD ? 4 : 2;        // first epilogue warp
     static constexpr int MMA_WARP = PROD ? 4 + EPI : 1;   // MMA issuer, owns TMEM
+    static constexpr int TMA8_WARP = MMA_WARP + 1;        // PROD = 2: the int8 TMA producer
     static constexpr int THREADS = PROD ? 32 * (4 + EPI + 4) : 64 + 32 * EPI;
     // arrivals that complete a stage's full barrier: the TMA producer's
-    // expect_tx, or one per producer warp of each CTA
-    static constexpr int FULL_ARRIVALS = PROD ? 4 * CG : 1;
+    // expect_tx, or one per producer (transform) warp of each CTA
+    static constexpr int FULL_ARRIVALS = PROD == 1 ? 4 * CG : (PROD == 2 ? XG_WARPS * CG : 1);
     // setmaxnreg shares of the PROD = 1 layout (launched at 65536 / THREADS)
     static constexpr int REGS_PRODUCER = 104, REGS_MMA = 48, REGS_EPILOGUE = 176;
-    static constexpr int STAGING_OFFSET = STAGES * STAGE_BYTES;
+    static constexpr int RING8_OFFSET = STAGES * STAGE_BYTES;
+    static constexpr int STAGING_OFFSET = RING8_OFFSET + RING8_BYTES;
     static constexpr int BAR_OFFSET = STAGING_OFFSET + STAGING_BYTES;
-    static constexpr int NUM_BARS = 2 * STAGES + 5;
+    static constexpr int NUM_BARS = 2 * STAGES + 5 + 2 * S8;
     static constexpr int USED = BAR_OFFSET + NUM_BARS * 8 + 16;
     // TMEM has 512 columns per SM: at most 512 / TMEM_COLS blocks may share an
     // SM, or a block would stall in tcgen05.alloc.  The shared-memory request
@@ -124,6 +143,8 @@ struct TcCfg {
                   "a CTA pair is a cluster of two splitting B's columns in halves");
     static_assert(!PROD || (INT_FOLD && EPI == 8 && B_COLS % 128 == 0),
                   "register-staged producer: int8 operands, two epilogue warpgroups");
+    static_assert(PROD != 2 || (S8 >= 2 && (XG == 1 || XG == 2) && B_COLS == 128),
+                  "staged producer: an int8 ring of two or more stages, one or two groups");
     static_assert(!PROD || 128 * (REGS_PRODUCER + REGS_MMA) + 32 * EPI * REGS_EPILOGUE <=
                                65536, "setmaxnreg shares exceed the block's registers");
     static_assert(!PROD || THREADS == 512, "launched at 128 registers a thread");
@@ -543,13 +564,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     uint8_t *smem = align_1024(smem_raw);
     uint8_t *sA = smem;
     uint8_t *sB = smem + STAGES * Cfg::A_BYTES;
+    uint8_t *sRing8 = smem + Cfg::RING8_OFFSET;  // PROD = 2: int8 stages
     uint8_t *sStage = smem + Cfg::STAGING_OFFSET;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + Cfg::BAR_OFFSET);
     uint64_t *empty = full + STAGES;
     uint64_t *acc_full = empty + STAGES;  // [2]
     uint64_t *acc_empty = acc_full + 2;   // [2]
     uint64_t *mma_done = acc_empty + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+    uint64_t *full8 = mma_done + 1;       // [S8]: an int8 stage has landed
+    uint64_t *empty8 = full8 + Cfg::S8;   // [S8]: an int8 stage has been widened
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(empty8 + Cfg::S8);
     __shared__ SlotPlan sp;  // this slot's list of work units
 
     const uint32_t warp = warp_id_uniform();
@@ -561,7 +585,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     if (warp == 0 && lane == 0) {
         sp.init(args, static_cast<int>(blockIdx.x) / Cfg::CM, static_cast<int>(gridDim.x) / Cfg::CM,
                 num_m_sched * args.num_n_tiles);
-        if constexpr (!Cfg::PROD) {
+        if constexpr (Cfg::PROD != 1) {
             prefetch_tmap(&tmap_a);
             prefetch_tmap(&tmap_b);
         }
@@ -578,6 +602,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             mbar_init(&acc_empty[b], Cfg::EPI * Cfg::CG);
         }
         mbar_init(mma_done, 1);
+        for (int s = 0; s < Cfg::S8; ++s) {
+            mbar_init(&full8[s], 1);                 // the int8 producer's expect_tx
+            mbar_init(&empty8[s], Cfg::XG_WARPS);    // the warps of the group that widens it
+        }
         fence_barrier_init();
     }
     if (warp == Cfg::MMA_WARP) {
@@ -605,7 +633,87 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     const int num_units = sp.units();
 
     if (Cfg::PROD ? warp < 4 : warp == 0) {
-        if constexpr (Cfg::PROD) {
+        if constexpr (Cfg::PROD == 2) {
+            // ------- int8 stages widened into fp16 stages (warps 0-3) -------
+            // Group g of XG takes the slot's K-tiles g, g + XG, ...  For each:
+            // wait until its int8 stage has landed and its fp16 slot has been
+            // read by the tensor core, widen the stage's 64-byte rows (A's 128,
+            // then B's 64-row boxes) into the fp16 slot's 128-byte rows with
+            // the 128-byte swizzle TMA would write, fence the stores into the
+            // async proxy, then release the int8 stage and arrive once per
+            // warp on the MMA issuer's full barrier (with a CTA pair the even
+            // CTA's, at cluster scope).  Thread t of a group takes the stage's
+            // 16-byte chunks t, t + TG, ...: each warp load reads 512
+            // consecutive bytes, and every 8-lane phase of a 16-byte store
+            // covers rows r and r + 1 of one 8-row swizzle group, 32 distinct
+            // banks.
+            setmaxnreg_dec<Cfg::REGS_PRODUCER>();
+            constexpr int TG = Cfg::XG_WARPS * 32;             // threads per group
+            constexpr int PER = Cfg::STAGE8_BYTES / 16 / TG;   // chunks per thread
+            static_assert(PER % 8 == 0, "chunks per thread");
+            const uint32_t g = warp / Cfg::XG_WARPS;
+            const uint32_t tg = (warp % Cfg::XG_WARPS) * 32u + lane;
+            const uint32_t x = (tg >> 2) & 7u;  // the swizzle of every row this thread writes
+            const uint32_t c2 = (tg & 3u) * 2u; // fp16 chunks c2, c2 + 1 of the row
+            const uint32_t lo_off = (c2 ^ x) << 4, hi_off = ((c2 + 1u) ^ x) << 4;
+            int total = 0;  // K-tiles of this slot
+            for (int u = 0; u < num_units; ++u) {
+                const WorkUnit w = sp.unit(u);
+                total += w.ke - w.kb;
+            }
+            bool ok = true;
+            for (int it = static_cast<int>(g); it < total; it += Cfg::XG) {
+                const uint32_t s8 = it % Cfg::S8, ph8 = (it / Cfg::S8) & 1u;
+                const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+                // every lane observes the int8 stage's completion (TMA bytes)
+                if (!mbar_wait(&full8[s8], ph8, ctx, kSiteConvertFull)) {
+                    ok = false;
+                    break;
+                }
+                bool fr = true;
+                if (lane == 0) fr = mbar_wait(&empty[s], ph ^ 1u, ctx, kSiteConvertEmpty);
+                if (__shfl_sync(0xffffffffu, fr ? 1 : 0, 0) == 0) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t src = smem_u32(sRing8 + s8 * Cfg::STAGE8_BYTES) + tg * 16u;
+                const uint32_t dA = smem_u32(sA + s * Cfg::A_BYTES);
+                const uint32_t dB = smem_u32(sB + s * Cfg::B_BYTES);
+#pragma unroll
+                for (int h = 0; h < PER; h += 8) {
+                    uint4 v[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) v[j] = lds_u4(src + (h + j) * TG * 16);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t r = (tg >> 2) + (h + j) * (TG / 4);  // 64-byte row
+                        const uint32_t row = r < BM ? dA + r * 128u : dB + (r - BM) * 128u;
+                        uint32_t o[8];
+                        widen16(v[j], o);
+                        sts128(row + lo_off, o[0], o[1], o[2], o[3]);
+                        sts128(row + hi_off, o[4], o[5], o[6], o[7]);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&empty8[s8]);
+                    if constexpr (Cfg::CG == 2)
+                        mbar_arrive_cluster(mapa_shared(smem_u32(&full[s]), 0));
+                    else
+                        mbar_arrive(&full[s]);
+                }
+            }
+            if constexpr (Cfg::CM > 1) {
+                // the last multicast releases of the fp16 ring land before the exit
+                if (threadIdx.x == 0)
+                    for (int i = 0; ok && i < STAGES; ++i) {
+                        const int t2 = total + i;
+                        ok = mbar_wait(&empty[t2 % STAGES], ((t2 / STAGES) & 1u) ^ 1u, ctx,
+                                       kSiteConvertEmpty);
+                    }
+            }
+        } else if constexpr (Cfg::PROD == 1) {
             // ------- producer: int8 loads widened in registers (warps 0-3) -------
             setmaxnreg_dec<Cfg::REGS_PRODUCER>();
             const RegProducer<Cfg> rp(threadIdx.x);
@@ -722,6 +830,38 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         }
     } else if (Cfg::PROD ? warp >= static_cast<uint32_t>(Cfg::MMA_WARP) : warp == 1) {
         if constexpr (Cfg::PROD) setmaxnreg_dec<Cfg::REGS_MMA>();  // the MMA warpgroup
+        if constexpr (Cfg::PROD == 2) {
+            if (warp == Cfg::TMA8_WARP && lane == 0) {
+                // ---------------- producer: int8 tiles by TMA into the int8 ring ----------------
+                // Each CTA loads its own 128 rows of A and B_COLS columns of B
+                // (two 64-byte-wide boxes) into its own int8 stage, counted on
+                // its own barrier; the bytes outside the matrices arrive as zeros.
+                uint32_t it = 0;
+                bool ok = true;
+                for (int u = 0; ok && u < num_units; ++u) {
+                    const WorkUnit w = sp.unit(u);
+                    int m0, n0;
+                    tile_origin(w.tile, num_m_sched, args.num_n_tiles, args.group_m, BM * Cfg::CM,
+                                BN, m0, n0);
+                    m0 += static_cast<int>(crank) * BM;
+                    const int nb = n0 + static_cast<int>(crank) * Cfg::B_COLS;
+                    for (int kt = w.kb; kt < w.ke; ++kt, ++it) {
+                        const uint32_t s8 = it % Cfg::S8, ph8 = (it / Cfg::S8) & 1u;
+                        if (!mbar_wait(&empty8[s8], ph8 ^ 1u, ctx, kSiteProducerEmpty)) {
+                            ok = false;
+                            break;
+                        }
+                        uint8_t *dst = sRing8 + s8 * Cfg::STAGE8_BYTES;
+                        mbar_arrive_expect_tx(&full8[s8], Cfg::STAGE8_BYTES);
+                        tma_load_2d(dst, &tmap_a, &full8[s8], kt * BK, m0);
+#pragma unroll
+                        for (int j = 0; j < Cfg::B_COLS / 64; ++j)
+                            tma_load_2d(dst + Cfg::A8_BYTES + j * (64 * BK), &tmap_b, &full8[s8],
+                                        nb + j * 64, kt * BK);
+                    }
+                }
+            }
+        }
         // with a CTA pair only the even CTA issues (its MMAs cover both CTAs)
         if (warp == Cfg::MMA_WARP && lane == 0 && (Cfg::CG == 1 || crank == 0)) {
             // ---------------- MMA issuer ----------------
@@ -1014,7 +1154,7 @@ static cudaError_t launch_tc(const P &p, cudaStream_t stream) {
     }
     lc.numAttrs = nattr;
     TcOperands ops{};
-    if constexpr (Cfg::PROD) {
+    if constexpr (Cfg::PROD != 0) {
         // setmaxnreg.inc waits until the block's pool can grant the
         // registers, and the pool is what the kernel was launched with:
         // launch only if the shares fit it, so that no warpgroup can wait
@@ -1026,6 +1166,8 @@ static cudaError_t launch_tc(const P &p, cudaStream_t stream) {
                                                     32 * Cfg::EPI * Cfg::REGS_EPILOGUE;
         }();
         if (!regs_fit) return cudaErrorInvalidConfiguration;
+    }
+    if constexpr (Cfg::PROD == 1) {
         ops.A = static_cast<const int8_t *>(p.a_ptr);
         ops.B = static_cast<const int8_t *>(p.b_ptr);
         ops.lda = p.lda;
@@ -1076,11 +1218,15 @@ static KernelInfo tc_info() {
     k.a_box_y = Cfg::BM;
     k.b_box_x = 64;
     k.b_box_y = Cfg::BK;
-    k.a_swizzle128 = k.b_swizzle128 = true;
+    // fp16 / bf16 boxes of 64 elements (128 bytes) land 128-byte swizzled;
+    // the staged producer's int8 boxes (64 bytes wide) land as plain rows
+    k.a_swizzle128 = k.b_swizzle128 = Cfg::PROD != 2;
     k.c_tma = true;
     k.kc = Cfg::KC;
     k.slabs_per_tile = Cfg::CM * Cfg::EPI;
-    k.producer = Cfg::PROD ? PGEMM_PRODUCER_REGISTERS : PGEMM_PRODUCER_TMA;
+    k.producer = Cfg::PROD == 1   ? PGEMM_PRODUCER_REGISTERS
+                 : Cfg::PROD == 2 ? PGEMM_PRODUCER_STAGED
+                                  : PGEMM_PRODUCER_TMA;
     k.schedule_slots = tc_slots<Cfg>;
     k.func = reinterpret_cast<const void *>(tc_gemm_kernel<Cfg>);
     return k;

@@ -67,6 +67,11 @@ def test_list_configs(L):
     # and widened in registers by the GEMM itself)
     i8_regs = [c for c in i8 if len(c) > 5 and c[5] == pg.PRODUCERS["registers"]]
     assert {(c[0], c[1], c[3]) for c in i8_regs} == {(256, 256, 4), (256, 256, 5), (256, 256, 6)}
+    # int8 on the CTA pair with int8 stages by TMA widened in shared memory
+    # (`stages` = depth of the int8 ring)
+    i8_staged = [c for c in i8 if len(c) > 5 and c[5] == pg.PRODUCERS["staged"]]
+    assert {(c[0], c[1], c[3]) for c in i8_staged} == {(256, 256, 4), (256, 256, 5), (256, 256, 6)}
+    assert not [c for c in f32 + bf16 if len(c) > 5 and c[5] == pg.PRODUCERS["staged"]]
     # the mma.sync int8 engine: 128 x 128 tiles, K-tiles of 128 int8
     imma = [c for c in i8 if len(c) > 6 and c[6] == pg.ENGINES["mma_sync"]]
     assert {(c[0], c[1], c[2]) for c in imma} == {(128, 128, 128)}
@@ -119,3 +124,18 @@ def test_stage_reuse_demo_validation_without_gpu(L):
     assert f(good, 4, 16, good, good, 1, 7, 0, None, 0, None) == 1      # no such warp
     assert f(good + 4, 4, 16, good, good, 1, -1, 0, None, 0, None) == 2  # misaligned X
     assert f(good, 0, 16, None, None, 1, -1, 0, None, 0, None) == 0      # nothing to do
+
+
+def test_config_struct_matches_the_header():
+    # the binding's pgemm_config has the header's fields, in the header's order
+    src = open(HEADER).read()
+    body = re.search(r"typedef struct \{(.*?)\} pgemm_config;", src, re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    names = []
+    for decl in body.split(";"):
+        decl = decl.strip()
+        if decl:
+            assert decl.startswith("int "), decl
+            names += [n.strip() for n in decl[4:].split(",")]
+    assert [f[0] for f in pg.Config._fields_] == names
+    assert ctypes.sizeof(pg.Config) == 4 * len(names)
