@@ -103,11 +103,20 @@ typedef enum { PGEMM_F32 = 0, PGEMM_BF16 = 1, PGEMM_I8 = 2 } pgemm_dtype;
  *     stage exactly to fp16 into a short ring of fp16 stages that the tensor
  *     core reads (shared memory to shared memory).  No widening pass runs and
  *     the operands cross L2 as int8; the MMA issuer and the exact-round
- *     epilogue are the default kernel's. */
+ *     epilogue are the default kernel's.
+ *   PGEMM_PRODUCER_WIDEN_IN_KERNEL (int8, CTA pair 256 x 256): the TMA ring of
+ *     PGEMM_PRODUCER_TMA, but the int8 -> fp16 widening of A and B runs inside
+ *     the GEMM instead of as a pass before it: four warps per CTA widen the
+ *     operands into the fp16 scratch one 64-wide K chunk after another, and
+ *     the TMA producer loads from a chunk once every CTA has published its
+ *     share of it, so the widening overlaps the main loop of the first tiles.
+ *     Needs K and N multiples of 16 (int8 rows 16-byte aligned); launched
+ *     cooperatively (every CTA resident). */
 typedef enum {
     PGEMM_PRODUCER_TMA = 0,
     PGEMM_PRODUCER_REGISTERS = 1,
-    PGEMM_PRODUCER_STAGED = 2
+    PGEMM_PRODUCER_STAGED = 2,
+    PGEMM_PRODUCER_WIDEN_IN_KERNEL = 3
 } pgemm_producer;
 
 /* Which multiply-accumulate consumes the stages (pgemm_config.engine).
@@ -230,11 +239,14 @@ PGEMM_API pgemm_status pgemm_kernel_attrs(pgemm_dtype dtype, const pgemm_config 
  * (cfg NULL = default configuration): output tiles (a CTA pair's 256-row tile
  * counts once), schedule slots (units that run at once), tiles split along K
  * and their parts (0 and 1 when nothing is split; for fp32, the stream-K
- * tiles and the most pieces one of them is spread over).  No GPU work is
- * enqueued.  Any output pointer may be NULL. */
+ * tiles and the most pieces one of them is spread over), and tiles run as two
+ * half-width units each (the 256-wide tensor-core tiles of a partial last
+ * wave, cut along N when they fit twice on the slots; then nothing is split
+ * along K).  No GPU work is enqueued.  Any output pointer may be NULL. */
 PGEMM_API pgemm_status pgemm_schedule(pgemm_dtype dtype, const pgemm_config *cfg, int M, int N,
                                       int K, long long *tiles, int *slots,
-                                      long long *split_tiles, int *parts);
+                                      long long *split_tiles, int *parts,
+                                      long long *half_tiles);
 
 /* The stream-K rule, a pure host computation (no device needed; the pages
  * have no counterpart).  `tiles` output tiles on `slots` schedule slots

@@ -36,7 +36,7 @@ STATUS = {
 NOALLOC_SCRATCH_BYTES = 32 << 20
 DTYPES = {"f32": 0, "bf16": 1, "i8": 2}
 # pgemm_producer: who fills the shared-memory stages
-PRODUCERS = {"tma": 0, "registers": 1, "staged": 2}
+PRODUCERS = {"tma": 0, "registers": 1, "staged": 2, "widen_in_kernel": 3}
 # pgemm_engine: which multiply-accumulate consumes the stages
 ENGINES = {"default": 0, "mma_sync": 1}
 # Every function include/pgemm.h declares.
@@ -103,7 +103,7 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
         "pgemm_status_string": [i],
         "pgemm_version": [],
         "pgemm_stage_reuse_demo": [vp, i, i, vp, vp, i, i, ctypes.c_uint, vp, i, vp],
-        "pgemm_schedule": [i, cfgp, i, i, i, llp, ip, llp, ip],
+        "pgemm_schedule": [i, cfgp, i, i, i, llp, ip, llp, ip, llp],
         "pgemm_stream_k_plan": [ll, i, i, i, llp, ip, ip, llp],
         "pgemm_trim_scratch": [],
     }
@@ -226,12 +226,16 @@ def pgemm_stage_reuse_demo(X, rows, cols, perm, out, check_reuse, delay_warp=-1,
 
 def pgemm_schedule(dtype: str, M: int, N: int, K: int, config=None):
     """The persistent schedule of a call on the current device: a dict with
-    tiles, slots (units running at once), split_tiles and parts."""
+    tiles, slots (units running at once), split_tiles and parts (split along
+    K), and half_tiles (tiles run as two half-width units)."""
     t, sl, st, p = ctypes.c_longlong(), ctypes.c_int(), ctypes.c_longlong(), ctypes.c_int()
+    ht = ctypes.c_longlong()
     _check(lib().pgemm_schedule(DTYPES[dtype], _cfg(config), M, N, K, ctypes.byref(t),
-                                ctypes.byref(sl), ctypes.byref(st), ctypes.byref(p)),
+                                ctypes.byref(sl), ctypes.byref(st), ctypes.byref(p),
+                                ctypes.byref(ht)),
            "pgemm_schedule")
-    return {"tiles": t.value, "slots": sl.value, "split_tiles": st.value, "parts": p.value}
+    return {"tiles": t.value, "slots": sl.value, "split_tiles": st.value, "parts": p.value,
+            "half_tiles": ht.value}
 
 
 def pgemm_stream_k_plan(tiles: int, slots: int, k_tiles: int, max_parts: int = 0):

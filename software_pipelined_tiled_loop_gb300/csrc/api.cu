@@ -211,13 +211,34 @@ static pgemm_config default_config(pgemm_dtype dt, int M, int N, int K, int sm_c
 // 2048^2 x 8192, where every slot would share: 65.0 against 57.3 without).
 constexpr int kTcMaxPieces = 2;
 
+// Half-width units instead (kernels with 256-wide tiles fed by TMA, the
+// library's default up to kHalvesMaxKTiles K-tiles): when the R leftover
+// tiles fit twice on the slots, each is cut along N into its left and right
+// 128 columns, 2R units of the full K range that exchange nothing (no
+// partial-sum memory, no counters), so the wave after them is never held up
+// by an exchange.  A half-width unit's N = 128 MMAs read A in full for half
+// the products, so per K-tile it costs more than half a whole tile; with
+// long K that outweighs the exchange it saves (bf16 4096^2: K = 512 24.6
+// against 26.6 us without a split, K = 2048 53.2 against 55.9 us with K
+// halves; K = 16384 328.7 against 311.8 us, and int8 4096^3 108.8 against
+// 106.2 us).  An explicit max_k_parts > 1 asks for stream-K pieces.
+// allow_k_split = false: a call that may not allocate (no exchange memory).
+constexpr int kHalvesMaxKTiles = 32;
 static TileSchedule plan_schedule(const KernelInfo &k, int M, int N, int K, int slots,
-                                  int max_parts) {
+                                  int max_parts, bool allow_k_split = true) {
     TileSchedule s;
     s.tiles = static_cast<long long>((M + k.bm - 1) / k.bm) * ((N + k.bn - 1) / k.bn);
     s.slots = slots;
     if (k.schedule_slots == nullptr) return s;
     const int T = (K + k.bk - 1) / k.bk;
+    if (k.halves && max_parts == 0 && T > 0 && T <= kHalvesMaxKTiles) {
+        const long long rem = s.tiles % slots;
+        if (rem > 0 && 2 * rem <= slots) {
+            s.half_tiles = rem;
+            return s;
+        }
+    }
+    if (!allow_k_split) return s;
     const int cap = max_parts > 0 ? max_parts : (k.stream_k ? 0 : kTcMaxPieces);
     long long share = 0;
     if (pgemm_stream_k_plan(s.tiles, slots, T, cap, &s.split_tiles, &s.sk_slots, &s.parts,
@@ -360,6 +381,10 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
             c.max_k_parts = cfg_in->max_k_parts;
             if (cfg_in->group_m > 0) c.group_m = cfg_in->group_m;
         }
+        // a call with fixed scratch widens by the pass: the in-kernel
+        // widening's chunk counters would need memory of their own
+        if (fixed_scratch != nullptr && c.producer == PGEMM_PRODUCER_WIDEN_IN_KERNEL)
+            c.producer = PGEMM_PRODUCER_TMA;
         k = find_kernel(DT, c);
         if (!k) return PGEMM_ERR_UNSUPPORTED_CONFIG;
         st = kernel_setup(*d, *k, &blocks_per_sm, &slots);
@@ -371,7 +396,7 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
     // scratch buffer does not split: the exchange area would need memory.
     TileSchedule sched;
     if (k->schedule_slots != nullptr)
-        sched = plan_schedule(*k, M, N, K, slots, fixed_scratch != nullptr ? 1 : c.max_k_parts);
+        sched = plan_schedule(*k, M, N, K, slots, c.max_k_parts, fixed_scratch == nullptr);
 
     // Operands as the kernels read them: element type, pitch, base pointer.
     // int8 is widened to fp16 by a pre-pass, except for the mma.sync engine,
@@ -383,6 +408,12 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
     // the staged producer's TMA copies the int8 operands as they are
     const bool staged = KIND == Kind::I8 && !imma && k->producer == PGEMM_PRODUCER_STAGED;
     const bool raw_i8 = rp || staged;  // the kernel reads int8 (no widening pass)
+    // widening inside the GEMM: fp16 scratch as for the pass, no pass
+    const bool fused = KIND == Kind::I8 && !imma && k->producer == PGEMM_PRODUCER_WIDEN_IN_KERNEL;
+    if (fused && (K % 16 != 0 || N % 16 != 0)) return PGEMM_ERR_UNSUPPORTED_CONFIG;
+    const bool widen_pass = KIND == Kind::I8 && !imma && !raw_i8 && !fused && K > 0;
+    const long long widen_chunks = fused ? (K + 63) / 64 : 0;  // at most this many K chunks
+    uint32_t *chunk_ready = nullptr;
     const int in_bytes = KIND == Kind::F32 ? 4 : ((imma || raw_i8) ? 1 : 2);
     const long long lda = K, ldb = N;
     const void *a_op = A;
@@ -392,18 +423,23 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
     scratch.s = stream;
     Scratch split_area;  // partial sums and counters of stream-K tiles
     split_area.s = stream;
-    if (sched.split_tiles > 0) {
+    if (sched.split_tiles > 0 || widen_chunks > 0) {
+        // [partial sums][stream-K counters][K-chunk counters of in-kernel widening]
         const long long pbytes = round_up(sched.partial_words * 4, 256);
-        const long long cbytes = round_up(sched.counter_words * 4, 256);
+        const long long cbytes = round_up((sched.counter_words + widen_chunks) * 4, 256);
         if (cudaMallocFromPoolAsync(&split_area.p, pbytes + cbytes, d->pool, stream) != cudaSuccess)
             return PGEMM_ERR_CUDA;
-        sched.partials = static_cast<uint32_t *>(split_area.p);
-        sched.counters = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(split_area.p) + pbytes);
+        uint32_t *counters =
+            reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(split_area.p) + pbytes);
+        if (sched.split_tiles > 0) {
+            sched.partials = static_cast<uint32_t *>(split_area.p);
+            sched.counters = counters;
+        }
+        if (widen_chunks > 0) chunk_ready = counters + sched.counter_words;
         // The counters start at zero: the int8 widening pass (which the GEMM
         // waits for) zeroes them; otherwise a memset before any pre-pass does,
         // so that a programmatic launch after the pre-pass still finds them zero.
-        if (!(KIND == Kind::I8 && k->engine == PGEMM_ENGINE_DEFAULT && !raw_i8 && K > 0) &&
-            cudaMemsetAsync(sched.counters, 0, cbytes, stream) != cudaSuccess)
+        if (!widen_pass && cudaMemsetAsync(counters, 0, cbytes, stream) != cudaSuccess)
             return PGEMM_ERR_CUDA;
     }
     std::function<cudaError_t()> prepass;  // repack / widening launch, if any
@@ -435,7 +471,8 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
             }
             // The pre-pass is launched below, after every tensor map is encoded,
             // so that the GEMM launch follows it with no host work in between.
-            prepass = [=, &d]() -> cudaError_t {
+            // With the widening inside the GEMM there is none.
+            if (!fused) prepass = [=, &d]() -> cudaError_t {
                 if (imma || raw_i8) {  // int8 to 16-byte pitches as needed; mma.sync: B -> B^T
                     cudaError_t e = cudaSuccess;
                     if (a_repack)
@@ -539,6 +576,8 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
         p.sm_count = d->sm_count; p.blocks_per_sm = blocks_per_sm;
         p.tmap_a = &ta; p.tmap_b = &tb; p.tmap_c = tmap_c; p.ctx = ctx;
         p.a_ptr = a_op; p.b_ptr = b_op; p.lda = a_ld; p.ldb = b_ld;
+        p.widen_src_a = A; p.widen_src_b = B; p.widen_lda = lda; p.widen_ldb = ldb;
+        p.widen_ready = chunk_ready;
         p.after_prepass = after_prepass;
         p.sched = sched;
         p.alpha = alpha; p.beta = beta; p.C = C;
@@ -702,7 +741,8 @@ pgemm_status pgemm_stream_k_plan(long long tiles, int slots, int k_tiles, int ma
 }
 
 pgemm_status pgemm_schedule(pgemm_dtype dtype, const pgemm_config *cfg, int M, int N, int K,
-                            long long *tiles, int *slots, long long *split_tiles, int *parts) {
+                            long long *tiles, int *slots, long long *split_tiles, int *parts,
+                            long long *half_tiles) {
     if (M < 0 || N < 0 || K < 0) return PGEMM_ERR_INVALID_VALUE;
     if (dtype != PGEMM_F32 && dtype != PGEMM_BF16 && dtype != PGEMM_I8) return PGEMM_ERR_INVALID_VALUE;
     std::lock_guard<std::mutex> lock(g_mu);
@@ -730,6 +770,7 @@ pgemm_status pgemm_schedule(pgemm_dtype dtype, const pgemm_config *cfg, int M, i
     if (slots) *slots = s.slots;
     if (split_tiles) *split_tiles = s.split_tiles;
     if (parts) *parts = s.parts;
+    if (half_tiles) *half_tiles = s.half_tiles;
     return PGEMM_OK;
 }
 

@@ -20,6 +20,7 @@ enum WaitSite : uint32_t {
     kSiteConvertEmpty = 8,    // int8 widening warps waiting for a free fp16 slot
     kSiteSelfTest = 9,        // pgemm_selftest_wait_timeout
     kSiteSplitPartial = 10,   // last piece of a stream-K tile waiting for the others' partials
+    kSiteWidenChunk = 11,     // TMA producer waiting for a K chunk widened inside the GEMM
 };
 
 // Problem description passed by value to every kernel.
@@ -39,8 +40,11 @@ struct GemmArgs {
     // two tiles.  The other tiles are whole units, tile R + j + i * G for
     // slot j of G.  The pieces of a tile meet through `partials` (raw partial
     // sums, one slab per slot and piece) and `counters` (zero at launch).
-    // None: split_tiles = 0.
+    // None: split_tiles = 0.  Alternatively the first half_tiles tiles are
+    // each cut into two half-width units (the tile's left and right BN / 2
+    // columns over all of K), on slots 0 .. 2 * half_tiles - 1: no exchange.
     int split_tiles, sk_slots;
+    int half_tiles;
     uint32_t *partials;
     uint32_t *counters;
 };

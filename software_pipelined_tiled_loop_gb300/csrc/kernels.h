@@ -32,6 +32,8 @@ struct TileSchedule {
     long long tiles = 0;
     int slots = 0;
     long long split_tiles = 0;
+    // leftover tiles run as two half-width units each instead (no exchange)
+    long long half_tiles = 0;
     int sk_slots = 0;
     int parts = 1;
     long long partial_words = 0, counter_words = 0;
@@ -56,6 +58,11 @@ struct LaunchCommon {
     // kernels whose threads load the operands themselves.
     const void *a_ptr, *b_ptr;
     long long lda, ldb;
+    // In-kernel widening: the caller's int8 operands (pitches in bytes), the
+    // destination being a_ptr / b_ptr above, and the per-chunk counters.
+    const void *widen_src_a, *widen_src_b;
+    long long widen_lda, widen_ldb;
+    uint32_t *widen_ready;
 };
 
 struct LaunchBf16 : LaunchCommon {
@@ -93,6 +100,10 @@ struct KernelInfo {
     // on pieces; the tensor-core kernels run them in-kernel, two counters per
     // tile and epilogue warp, at most two pieces a tile by default.
     bool stream_k = false;
+    // The kernel can run a tile as two half-width units (BN = 256 tensor-core
+    // kernels fed by TMA): the leftover tiles of a partial last wave are then
+    // cut along N, into 2R units on as many slots, rather than along K.
+    bool halves = false;
     cudaError_t (*schedule_slots)(const LaunchCommon &, int *slots) = nullptr;
     const void *func = nullptr;
     const void *aux_func = nullptr;  // a second kernel of the same launch (same attributes)

@@ -431,6 +431,14 @@ __device__ __forceinline__ void grid_launch_dependents() {
 // Release increment: every memory operation this thread performed (and, via
 // a preceding warp or block barrier, those of the threads it synchronised
 // with) is visible to a thread that acquire-reads the new value.
+// Orders this thread's generic-proxy accesses to global memory with its
+// async-proxy ones (TMA): between global stores another CTA's TMA copies
+// will read and the release that publishes them, and between the acquire
+// that observes them and those TMA copies.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ void red_release_add(uint32_t *p, uint32_t v) {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }

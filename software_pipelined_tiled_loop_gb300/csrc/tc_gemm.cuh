@@ -80,6 +80,11 @@ namespace pg {
 // core reads (shared memory to shared memory) in XG groups that take
 // alternate K-tiles.  No widening pass, and the int8 operands cross L2 once
 // at half the fp16 bytes.
+// 3: the widening pass runs inside the GEMM: warps 0-3 of every CTA widen
+// their share of A and B into the fp16 copies, one 64-wide K chunk after
+// another, while one lane of warp 4 + EPI + 1 fills the ring by TMA from
+// those copies as in 0, waiting for each K chunk to be complete in every
+// CTA before it loads from it (FusedWiden).
 template <int BN_, int STAGES_, int KC_, int BF16_, bool INT_FOLD_, int EPI_ = 4, int CM_ = 1,
           int CG_ = 1, int PROD_ = 0, int S8_ = 0, int XG_ = 1>
 struct TcCfg {
@@ -95,6 +100,10 @@ struct TcCfg {
     static constexpr int B_BYTES = B_COLS * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // per CTA
     static constexpr int TX_BYTES = STAGE_BYTES * CG;      // counted on the MMA's full barrier
+    // a half-width unit (BN = 256 tiles: columns [128 h, 128 h + 128) only)
+    static constexpr int STAGE_BYTES_HALF = A_BYTES + B_BYTES / 2;
+    static constexpr int TX_BYTES_HALF = STAGE_BYTES_HALF * CG;
+    static constexpr bool HALVES = BN_ == 256 && (PROD_ == 0 || PROD_ == 3);
     // PROD = 2: the int8 staging ring (A 128 x 64 bytes, then B as B_COLS/64
     // boxes of 64 k-rows x 64 bytes; 64-byte rows, unswizzled).
     static constexpr int S8 = PROD_ == 2 ? S8_ : 0;
@@ -116,13 +125,15 @@ struct TcCfg {
     static constexpr int PROD = PROD_;
     static constexpr int EPI_WARP0 = PROD ? 4 : 2;        // first epilogue warp
     static constexpr int MMA_WARP = PROD ? 4 + EPI : 1;   // MMA issuer, owns TMEM
-    static constexpr int TMA8_WARP = MMA_WARP + 1;        // PROD = 2: the int8 TMA producer
+    static constexpr int TMA8_WARP = MMA_WARP + 1;        // PROD = 2, 3: the TMA producer
     static constexpr int THREADS = PROD ? 32 * (4 + EPI + 4) : 64 + 32 * EPI;
     // arrivals that complete a stage's full barrier: the TMA producer's
     // expect_tx, or one per producer (transform) warp of each CTA
     static constexpr int FULL_ARRIVALS = PROD == 1 ? 4 * CG : (PROD == 2 ? XG_WARPS * CG : 1);
     // setmaxnreg shares of the PROD = 1 layout (launched at 65536 / THREADS)
     static constexpr int REGS_PRODUCER = 104, REGS_MMA = 48, REGS_EPILOGUE = 176;
+    static constexpr int WIDEN_DEPTH = 6;  // PROD = 3: widening steps in flight per thread
+    static constexpr int WIDEN_CHUNK = 256; // PROD = 3: K chunk (elements) published at once
     static constexpr int RING8_OFFSET = STAGES * STAGE_BYTES;
     static constexpr int STAGING_OFFSET = RING8_OFFSET + RING8_BYTES;
     static constexpr int BAR_OFFSET = STAGING_OFFSET + STAGING_BYTES;
@@ -143,6 +154,7 @@ struct TcCfg {
                   "a CTA pair is a cluster of two splitting B's columns in halves");
     static_assert(!PROD || (INT_FOLD && EPI == 8 && B_COLS % 128 == 0),
                   "register-staged producer: int8 operands, two epilogue warpgroups");
+    static_assert(WIDEN_CHUNK % BK == 0, "a K chunk holds whole K-tiles");
     static_assert(PROD != 2 || (S8 >= 2 && (XG == 1 || XG == 2) && B_COLS == 128),
                   "staged producer: an int8 ring of two or more stages, one or two groups");
     static_assert(!PROD || 128 * (REGS_PRODUCER + REGS_MMA) + 32 * EPI * REGS_EPILOGUE <=
@@ -230,30 +242,37 @@ __device__ __forceinline__ void release_acc(uint64_t *acc_empty_bar) {
 // list) and slab0 the slab of the tile's piece 0.  Pieces 1, 2, ... start
 // inside the tile, so each is its slot's first piece: slab (first slot + j)
 // * 2; piece 0 is its slot's second piece when that slot began in the tile
-// before.
+// before.  half >= 0: a half-width unit, only the tile's columns
+// [half * BN / 2, (half + 1) * BN / 2) over all of K.
 struct WorkUnit {
-    int tile, kb, ke, part, parts, slab, slab0;
+    int tile, kb, ke, part, parts, slab, slab0, half;
 };
 
-// A slot's list of work units (GemmArgs: the stream-K schedule): first its
-// stream-K pieces (at most two), then its whole tiles.  Producer, MMA issuer
-// and epilogue walk the same list.  Held in shared memory and written once,
-// with the pieces decoded in full there, so that walking the list costs no
-// 64-bit divisions (and no registers) in the loops.
+// A slot's list of work units (GemmArgs: the schedule of the leftover
+// tiles): first its stream-K pieces (at most two) or its half-width unit,
+// then its whole tiles.  Producer, MMA issuer and epilogue walk the same
+// list.  Held in shared memory and written once, with the pieces decoded in
+// full there, so that walking the list costs no 64-bit divisions (and no
+// registers) in the loops.
 struct SlotPlan {
     int T, R, G, j;
-    int n_sk, n_whole;
+    int n_sk, n_half, n_whole;
     WorkUnit piece[2];
 
     template <typename A>
     __device__ __forceinline__ void init(const A &a, int slot, int slots, int tiles) {
         T = a.num_k_tiles;
-        R = a.split_tiles;
+        // the leftover tiles [0, R) are split along K (stream-K pieces) or
+        // along N (two half-width units each, on slots 0 .. 2R - 1); the
+        // whole tiles are R + j, R + j + G, ...
+        R = a.split_tiles + a.half_tiles;
         G = slots;
         j = slot;
+        n_half = a.half_tiles > 0 && slot < 2 * a.half_tiles ? 1 : 0;
+        const int Rk = a.split_tiles;
         const int Gs = a.sk_slots;
-        const long long total = static_cast<long long>(R) * T;
-        const bool in_sk = R > 0 && slot < Gs;
+        const long long total = static_cast<long long>(Rk) * T;
+        const bool in_sk = Rk > 0 && slot < Gs;
         const long long sk_a = in_sk ? slot * total / Gs : 0;
         const long long sk_end = in_sk ? (slot + 1) * total / Gs : 0;
         n_sk = sk_end == sk_a ? 0 : ((sk_a / T) == ((sk_end - 1) / T) ? 1 : 2);
@@ -272,21 +291,28 @@ struct SlotPlan {
             w.parts = last - first + 1;
             w.slab = slot * 2 + u;
             w.slab0 = first * 2 + (first * total / Gs < t0 ? 1 : 0);
+            w.half = -1;
         }
         const int whole = tiles - R;
         n_whole = slot < whole ? (whole - slot + slots - 1) / slots : 0;
     }
-    __device__ __forceinline__ int units() const { return n_sk + n_whole; }
+    __device__ __forceinline__ int units() const { return n_sk + n_half + n_whole; }
     __device__ __forceinline__ WorkUnit unit(int u) const {
         if (u < n_sk) return piece[u];
         WorkUnit w;
-        w.tile = R + j + (u - n_sk) * G;
         w.kb = 0;
         w.ke = T;
         w.part = -1;
         w.parts = 1;
         w.slab = 0;
         w.slab0 = 0;
+        w.half = -1;
+        if (u < n_sk + n_half) {
+            w.tile = j >> 1;
+            w.half = j & 1;
+            return w;
+        }
+        w.tile = R + j + (u - n_sk - n_half) * G;
         return w;
     }
 };
@@ -431,12 +457,119 @@ struct SplitSlab {
 };
 
 // The int8 operands as stored by the caller, for the register-staged
-// producer: row-major, pitches in elements (bytes), rows 16-byte aligned.
+// producer and the in-kernel widening: row-major, pitches in elements
+// (bytes), rows 16-byte aligned.  In-kernel widening (PROD = 3) also: the
+// fp16 copies it writes (the TMA maps' sources) and the per-chunk counters.
 struct TcOperands {
     const int8_t *A;
     const int8_t *B;
     long long lda, ldb;
+    __half *A16, *B16;
+    long long lda16, ldb16;
+    uint32_t *ready;  // one per 64-wide K chunk, zero at launch
 };
+
+// In-kernel widening (PROD = 3), run by the 128 threads of warps 0-3 of
+// every CTA (global widening thread g of T = 128 * gridDim.x).  K chunk c is
+// A's columns [KW c, KW c + KW) and B's rows [KW c, KW c + KW), cut into
+// 16-byte pieces: A's M rows of w/16 pieces each, then B's w rows of N/16
+// pieces (w = the chunk's width, KW but for a narrower last chunk; K and N
+// are multiples of 16).  Each step a thread widens two pieces, g + (2 sub + j) T
+// for j = 0, 1, of the chunk's ceil(pieces / 2T) steps, so all lanes of a
+// warp finish a chunk together: the warp then fences and adds one to the
+// chunk's counter (release, GPU scope).  The chunk is complete when the
+// counter reaches 4 * gridDim.x.  Steps are software-pipelined D deep: the
+// loads of step s + D - 1 are issued before step s is converted and stored,
+// so that D steps of loads are in flight per thread.  Consecutive lanes take
+// consecutive pieces: a warp reads 64-byte row segments of A (or 512
+// contiguous bytes of B) and writes whole 128-byte lines.
+template <int D, int KW>
+__device__ __forceinline__ void fused_widen(const TcOperands &op, int M, int N, int K,
+                                            uint32_t g, uint32_t T) {
+    const int nchunks = (K + KW - 1) / KW;
+    if (nchunks == 0) return;
+    const long long npb = N / 16;  // pieces per B row
+    const int w_last = K - (nchunks - 1) * KW;
+    const long long TT = 2LL * T;
+    const long long p_full = (KW / 16LL) * M + KW * npb;
+    const long long p_last = static_cast<long long>(w_last / 16) * M + w_last * npb;
+    const int spc_full = static_cast<int>((p_full + TT - 1) / TT);
+    const int spc_last = static_cast<int>((p_last + TT - 1) / TT);
+    const int nsteps = (nchunks - 1) * spc_full + spc_last;
+    // step s -> (chunk, step within the chunk)
+    auto locate = [&](int s, int &c, int &sub) {
+        c = s < (nchunks - 1) * spc_full ? s / spc_full : nchunks - 1;
+        sub = s - c * spc_full;
+    };
+    // piece j of step s: source and destination, or false if past the chunk
+    auto piece = [&](int c, int sub, int j, const int8_t *&src, __half *&dst) -> bool {
+        const bool last = c == nchunks - 1;
+        const long long pa = last ? w_last / 16 : KW / 16;
+        const long long rows_b = last ? w_last : KW;
+        const long long i = g + (2LL * sub + j) * T;
+        if (i < pa * M) {
+            const long long r = i / pa, q = i - r * pa;
+            src = op.A + r * op.lda + static_cast<long long>(KW) * c + 16 * q;
+            dst = op.A16 + r * op.lda16 + static_cast<long long>(KW) * c + 16 * q;
+            return true;
+        }
+        const long long i2 = i - pa * M;
+        if (i2 >= rows_b * npb) return false;
+        const long long rb = i2 / npb, q = i2 - rb * npb;
+        const long long r = static_cast<long long>(KW) * c + rb;
+        src = op.B + r * op.ldb + 16 * q;
+        dst = op.B16 + r * op.ldb16 + 16 * q;
+        return true;
+    };
+    auto load = [&](int s, uint4 (&v)[2]) {
+        int c, sub;
+        locate(s, c, sub);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int8_t *src;
+            __half *dst;
+            v[j] = make_uint4(0u, 0u, 0u, 0u);
+            if (piece(c, sub, j, src, dst)) v[j] = ldg_nc_v4(src);
+        }
+    };
+    auto store = [&](int s, const uint4 (&v)[2]) {
+        int c, sub;
+        locate(s, c, sub);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int8_t *src;
+            __half *dst;
+            if (piece(c, sub, j, src, dst)) {
+                uint32_t o[8];
+                widen16(v[j], o);
+                uint4 *d = reinterpret_cast<uint4 *>(dst);
+                d[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                d[1] = make_uint4(o[4], o[5], o[6], o[7]);
+            }
+        }
+        if (sub == (c == nchunks - 1 ? spc_last : spc_full) - 1) {
+            // this warp's share of chunk c is written: publish it
+            __threadfence();
+            fence_proxy_async_global();
+            __syncwarp();
+            if ((threadIdx.x & 31u) == 0) red_release_add(op.ready + c, 1u);
+        }
+    };
+    uint4 x[D][2];
+#pragma unroll
+    for (int d = 0; d < D - 1; ++d)
+        if (d < nsteps) load(d, x[d]);
+    for (int s0 = 0; s0 < nsteps; s0 += D) {
+#pragma unroll
+        for (int d = 0; d < D; ++d) {
+            const int s = s0 + d;
+            if (s < nsteps) {
+                if (s + D - 1 < nsteps) load(s + D - 1, x[(d + D - 1) % D]);
+                store(s, x[d]);
+            }
+        }
+    }
+}
 
 // Register-staged int8 producer (PROD = 1), run by the 128 threads of warps
 // 0-3 of each CTA.  For every K-tile of the slot's units it loads this CTA's
@@ -632,8 +765,70 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     const uint32_t crank = Cfg::CM > 1 ? cluster_ctarank() : 0u;
     const int num_units = sp.units();
 
+    // ---------------- producer: TMA into the stage ring ----------------
+    // One lane runs it: warp 0 (PROD = 0), or warp MMA_WARP + 1 (PROD = 3),
+    // where chunk_ready(kt) first waits until K chunk kt of the operands has
+    // been widened by every CTA.
+    auto tma_producer = [&](auto &&chunk_ready) {
+        uint32_t it = 0;
+        bool ok = true;
+        for (int u = 0; ok && u < num_units; ++u) {
+            const WorkUnit w = sp.unit(u);
+            int m0, n0;
+            tile_origin(w.tile, num_m_sched, args.num_n_tiles, args.group_m, BM * Cfg::CM, BN, m0,
+                        n0);
+            m0 += static_cast<int>(crank) * BM;
+            for (int kt = w.kb; kt < w.ke; ++kt, ++it) {
+                const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+                if (!mbar_wait(&empty[s], ph ^ 1u, ctx, kSiteProducerEmpty) || !chunk_ready(kt)) {
+                    ok = false;
+                    break;
+                }
+                // a half-width unit loads half of this CTA's B columns: those
+                // of the unit's half of the tile
+                const bool hf = Cfg::HALVES && w.half >= 0;
+                const int b_cols = hf ? Cfg::B_COLS / 2 : Cfg::B_COLS;
+                const int nb = n0 + (hf ? w.half * (BN / 2) : 0) + static_cast<int>(crank) * b_cols;
+                if constexpr (Cfg::CG == 2) {
+                    // Both CTAs load their A rows and B columns into their own
+                    // shared memory; the bytes are counted on the even CTA's
+                    // full barrier, which its producer arms for both.
+                    const uint32_t full_lead = mapa_shared(smem_u32(&full[s]), 0);
+                    if (crank == 0)
+                        mbar_arrive_expect_tx(&full[s], hf ? Cfg::TX_BYTES_HALF : Cfg::TX_BYTES);
+                    tma_load_2d_pair(sA + s * Cfg::A_BYTES, &tmap_a, full_lead, kt * BK, m0);
+                    for (int j = 0; j < b_cols / 64; ++j)
+                        tma_load_2d_pair(sB + s * Cfg::B_BYTES + j * (BK * 128), &tmap_b,
+                                         full_lead, nb + j * 64, kt * BK);
+                    continue;
+                }
+                mbar_arrive_expect_tx(&full[s], hf ? Cfg::STAGE_BYTES_HALF : Cfg::STAGE_BYTES);
+                tma_load_2d(sA + s * Cfg::A_BYTES, &tmap_a, &full[s], kt * BK, m0);
+                for (int j = 0; j < b_cols / 64; ++j)
+                    tma_load_2d(sB + s * Cfg::B_BYTES + j * (BK * 128), &tmap_b, &full[s],
+                                nb + j * 64, kt * BK);
+            }
+        }
+        if constexpr (Cfg::CM > 1) {
+            // Producer tail: wait for the last release of every stage.  Those
+            // are the pair MMA issuer's multicast arrivals on this CTA's
+            // barriers, so none can land after the cluster has been left.
+            for (int i = 0; ok && i < STAGES; ++i, ++it) {
+                const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
+                ok = mbar_wait(&empty[s], ph ^ 1u, ctx, kSiteProducerEmpty);
+            }
+        }
+    };
+
+
     if (Cfg::PROD ? warp < 4 : warp == 0) {
-        if constexpr (Cfg::PROD == 2) {
+        if constexpr (Cfg::PROD == 3) {
+            // ------- the widening pass, inside the GEMM (warps 0-3) -------
+            setmaxnreg_dec<Cfg::REGS_PRODUCER>();
+            fused_widen<Cfg::WIDEN_DEPTH, Cfg::WIDEN_CHUNK>(ops, args.M, args.N, args.K,
+                                                            blockIdx.x * 128u + threadIdx.x,
+                                                            gridDim.x * 128u);
+        } else if constexpr (Cfg::PROD == 2) {
             // ------- int8 stages widened into fp16 stages (warps 0-3) -------
             // Group g of XG takes the slot's K-tiles g, g + XG, ...  For each:
             // wait until its int8 stage has landed and its fp16 slot has been
@@ -780,56 +975,26 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     }
             }
         } else if (lane == 0) {
-            // ---------------- producer: TMA into the stage ring ----------------
-            uint32_t it = 0;
-            bool ok = true;
-            for (int u = 0; ok && u < num_units; ++u) {
-                const WorkUnit w = sp.unit(u);
-                int m0, n0;
-                tile_origin(w.tile, num_m_sched, args.num_n_tiles, args.group_m, BM * Cfg::CM, BN, m0,
-                            n0);
-                m0 += static_cast<int>(crank) * BM;
-                for (int kt = w.kb; kt < w.ke; ++kt, ++it) {
-                    const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-                    if (!mbar_wait(&empty[s], ph ^ 1u, ctx, kSiteProducerEmpty)) {
-                        ok = false;
-                        break;
-                    }
-                    if constexpr (Cfg::CG == 2) {
-                        // Both CTAs load their A rows and B columns into their own
-                        // shared memory; the bytes are counted on the even CTA's
-                        // full barrier, which its producer arms for both.
-                        const uint32_t full_lead = mapa_shared(smem_u32(&full[s]), 0);
-                        if (crank == 0) mbar_arrive_expect_tx(&full[s], Cfg::TX_BYTES);
-                        tma_load_2d_pair(sA + s * Cfg::A_BYTES, &tmap_a, full_lead, kt * BK, m0);
-#pragma unroll
-                        for (int j = 0; j < Cfg::B_COLS / 64; ++j)
-                            tma_load_2d_pair(sB + s * Cfg::B_BYTES + j * (BK * 128), &tmap_b,
-                                             full_lead,
-                                             n0 + static_cast<int>(crank) * Cfg::B_COLS + j * 64,
-                                             kt * BK);
-                        continue;
-                    }
-                    mbar_arrive_expect_tx(&full[s], Cfg::STAGE_BYTES);
-                    tma_load_2d(sA + s * Cfg::A_BYTES, &tmap_a, &full[s], kt * BK, m0);
-#pragma unroll
-                    for (int j = 0; j < BN / 64; ++j)
-                        tma_load_2d(sB + s * Cfg::B_BYTES + j * (BK * 128), &tmap_b, &full[s],
-                                    n0 + j * 64, kt * BK);
-                }
-            }
-            if constexpr (Cfg::CM > 1) {
-                // Producer tail: wait for the last release of every stage.  Those
-                // are the pair MMA issuer's multicast arrivals on this CTA's
-                // barriers, so none can land after the cluster has been left.
-                for (int i = 0; ok && i < STAGES; ++i, ++it) {
-                    const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-                    ok = mbar_wait(&empty[s], ph ^ 1u, ctx, kSiteProducerEmpty);
-                }
-            }
+            tma_producer([](int) { return true; });
         }
     } else if (Cfg::PROD ? warp >= static_cast<uint32_t>(Cfg::MMA_WARP) : warp == 1) {
         if constexpr (Cfg::PROD) setmaxnreg_dec<Cfg::REGS_MMA>();  // the MMA warpgroup
+        if constexpr (Cfg::PROD == 3) {
+            if (warp == Cfg::TMA8_WARP && lane == 0) {
+                // K chunks complete in order for every warp that widens, so
+                // chunk kt complete means every chunk before it is too
+                int ready_upto = 0;
+                const uint32_t target = 4u * gridDim.x;
+                tma_producer([&](int kt) -> bool {
+                    const int c = kt * BK / Cfg::WIDEN_CHUNK;  // the K chunk holding K-tile kt
+                    if (c < ready_upto) return true;
+                    if (!wait_counter(ops.ready + c, target, ctx, kSiteWidenChunk)) return false;
+                    fence_proxy_async_global();  // the TMA copies below read what was published
+                    ready_upto = c + 1;
+                    return true;
+                });
+            }
+        }
         if constexpr (Cfg::PROD == 2) {
             if (warp == Cfg::TMA8_WARP && lane == 0) {
                 // ---------------- producer: int8 tiles by TMA into the int8 ring ----------------
@@ -865,8 +1030,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         // with a CTA pair only the even CTA issues (its MMAs cover both CTAs)
         if (warp == Cfg::MMA_WARP && lane == 0 && (Cfg::CG == 1 || crank == 0)) {
             // ---------------- MMA issuer ----------------
-            constexpr uint32_t idesc = idesc_f16(BM * Cfg::CG, BN, Cfg::BF16, /*A K-major*/ 0,
-                                                 /*B N-major*/ 1);
+            constexpr uint32_t idesc_full = idesc_f16(BM * Cfg::CG, BN, Cfg::BF16, /*A K-major*/ 0,
+                                                      /*B N-major*/ 1);
+            constexpr uint32_t idesc_half = idesc_f16(BM * Cfg::CG, BN / 2, Cfg::BF16, 0, 1);
             constexpr uint16_t kPair = 3;  // both CTAs of the pair
             uint32_t it = 0, gr = 0;
             bool ok = true;
@@ -874,6 +1040,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 const WorkUnit w = sp.unit(u);
                 const int kct = unit_round_tiles<Cfg>(w);
                 const int rounds = unit_rounds<Cfg>(w);
+                // a half-width unit: N = BN / 2 into the accumulator's first columns
+                const uint32_t idesc = (Cfg::HALVES && w.half >= 0) ? idesc_half : idesc_full;
                 for (int r = 0; ok && r < rounds; ++r, ++gr) {
                     const uint32_t ab = gr & 1u, aph = (gr >> 1) & 1u;
                     if (!mbar_wait(&acc_empty[ab], aph ^ 1u, ctx, kSiteMmaAccEmpty)) {
@@ -947,17 +1115,23 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         // The unit's place in C: rows [m_base, m_base + 32) of this warp's
         // quadrant, columns from n0 (rows below C take no part, and a
         // stream-K piece there exchanges nothing: the same for every piece).
+        // A half-width unit's accumulator columns [0, BN / 2) are C's columns
+        // from n0 + half * BN / 2; warps whose columns lie beyond BN / 2 have
+        // nothing of it (idle()), but still pass each accumulator back.
         auto place = [&](const WorkUnit &w, int &m_base, int &n0, bool &in_range, bool &split) {
             int m0;
             tile_origin(w.tile, num_m_sched, args.num_n_tiles, args.group_m, BM * Cfg::CM, BN, m0, n0);
+            if (Cfg::HALVES && w.half >= 0) n0 += w.half * (BN / 2);
             m0 += static_cast<int>(crank) * BM;
             in_range = m0 < args.M;  // the second tile of a pair may lie below C
             m_base = m0 + static_cast<int>(q * 32);
             split = w.part >= 0 && in_range;
         };
+        auto idle = [&](const WorkUnit &w) { return Cfg::HALVES && w.half >= 0 && col0 >= BN / 2; };
         for (int u = 0; ok && u < num_units; ++u) {
             if constexpr (Cfg::INT_FOLD) {
                 const int rounds = unit_rounds<Cfg>(sp.unit(u));
+                const bool no_cols = idle(sp.unit(u));
                 // Exact int8: sum the rounds' integer-valued fp32 partials in
                 // int32.  Rounds of at most 256 products (|x| <= 2^22) convert
                 // with one FADD: for an integer-valued x with |x| <= 2^22,
@@ -980,17 +1154,20 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     tc_fence_after();
                     const uint32_t t_row =
                         tmem_base + ((q * 32u) << 16) + ab * Cfg::ACC_COLS + col0;
+                    if (!no_cols) {
 #pragma unroll
-                    for (int c = 0; c < Cfg::EPI_COLS; c += 16) {
-                        uint32_t v[16];
-                        tmem_ld_32x32b_x16(t_row + c, v);
-                        tmem_ld_wait();
+                        for (int c = 0; c < Cfg::EPI_COLS; c += 16) {
+                            uint32_t v[16];
+                            tmem_ld_32x32b_x16(t_row + c, v);
+                            tmem_ld_wait();
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            if constexpr (kMagicFold)
-                                acc[c + j] += __float_as_uint(__uint_as_float(v[j]) + kMagic);
-                            else
-                                acc[c + j] += static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[j])));
+                            for (int j = 0; j < 16; ++j) {
+                                if constexpr (kMagicFold)
+                                    acc[c + j] += __float_as_uint(__uint_as_float(v[j]) + kMagic);
+                                else
+                                    acc[c + j] +=
+                                        static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[j])));
+                            }
                         }
                     }
                     tc_fence_before();
@@ -1008,6 +1185,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 int m_base, n0;
                 bool in_range, split;
                 place(w, m_base, n0, in_range, split);
+                if (no_cols) continue;
                 if (split) {
                     const SplitSlab<Cfg> slab(args, sp, w, crank, e);
                     if (!slab.last) {
@@ -1036,6 +1214,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     const uint32_t ab = gr & 1u, aph = (gr >> 1) & 1u;
                     if (!mbar_wait(&acc_full[ab], aph, ctx, kSiteEpilogueFull)) break;
                     tc_fence_after();
+                    if (idle(w)) {
+                        // none of this half-width unit's columns is this warp's
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) release_acc<Cfg>(&acc_empty[ab]);
+                        ++gr;
+                        continue;
+                    }
                     const uint32_t t_row =
                         tmem_base + ((q * 32u) << 16) + ab * Cfg::ACC_COLS + col0;
                     // role in a stream-K tile: store a partial, or add them all
@@ -1068,7 +1254,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     }
                     if (role == 1) slab.publish(args);
                     ++gr;
-                } else {
+                } else if (!idle(w)) {
                     // K == 0: C = beta * C, tensor memory is never read
                     uint32_t zero[32];
 #pragma unroll
@@ -1119,6 +1305,7 @@ static cudaError_t launch_tc(const P &p, cudaStream_t stream) {
     a.c_tma = p.tmap_c != nullptr ? 1 : 0;
     const TileSchedule &sc = p.sched;
     a.split_tiles = static_cast<int>(sc.split_tiles);
+    a.half_tiles = static_cast<int>(sc.half_tiles);
     a.sk_slots = sc.sk_slots;
     a.partials = sc.partials;
     a.counters = sc.counters;
@@ -1126,7 +1313,7 @@ static cudaError_t launch_tc(const P &p, cudaStream_t stream) {
     // After a pre-pass of this call, launch with programmatic stream
     // serialisation: the prologue overlaps the pre-pass's tail, and every
     // thread waits for it (grid_dependency_wait) before touching memory.
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[3];
     int nattr = 0;
     if (p.after_prepass) {
         attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1141,7 +1328,7 @@ static cudaError_t launch_tc(const P &p, cudaStream_t stream) {
     // one CTA (or CTA pair) per schedule slot, at most one per work unit
     // every slot when pieces are dealt out (the plan is made for sc.slots),
     // else at most one slot per tile
-    const long long units = sc.split_tiles > 0 ? sc.slots : sc.tiles;
+    const long long units = sc.split_tiles > 0 ? sc.slots : sc.tiles + sc.half_tiles;
     const int grid_units = static_cast<int>(units < sc.slots ? units : sc.slots);
     if (grid_units < 1) return cudaSuccess;
     lc.gridDim = dim3(Cfg::CM * grid_units);
@@ -1166,6 +1353,22 @@ static cudaError_t launch_tc(const P &p, cudaStream_t stream) {
                                                     32 * Cfg::EPI * Cfg::REGS_EPILOGUE;
         }();
         if (!regs_fit) return cudaErrorInvalidConfiguration;
+    }
+    if constexpr (Cfg::PROD == 3) {
+        // every CTA's widening feeds every CTA's loads: all must be resident
+        attr[nattr].id = cudaLaunchAttributeCooperative;
+        attr[nattr].val.cooperative = 1;
+        ++nattr;
+        lc.numAttrs = nattr;
+        ops.A = static_cast<const int8_t *>(p.widen_src_a);
+        ops.B = static_cast<const int8_t *>(p.widen_src_b);
+        ops.lda = p.widen_lda;
+        ops.ldb = p.widen_ldb;
+        ops.A16 = static_cast<__half *>(const_cast<void *>(p.a_ptr));
+        ops.B16 = static_cast<__half *>(const_cast<void *>(p.b_ptr));
+        ops.lda16 = p.lda;
+        ops.ldb16 = p.ldb;
+        ops.ready = p.widen_ready;
     }
     if constexpr (Cfg::PROD == 1) {
         ops.A = static_cast<const int8_t *>(p.a_ptr);
@@ -1226,8 +1429,10 @@ static KernelInfo tc_info() {
     k.slabs_per_tile = Cfg::CM * Cfg::EPI;
     k.producer = Cfg::PROD == 1   ? PGEMM_PRODUCER_REGISTERS
                  : Cfg::PROD == 2 ? PGEMM_PRODUCER_STAGED
+                 : Cfg::PROD == 3 ? PGEMM_PRODUCER_WIDEN_IN_KERNEL
                                   : PGEMM_PRODUCER_TMA;
     k.schedule_slots = tc_slots<Cfg>;
+    k.halves = Cfg::HALVES;
     k.func = reinterpret_cast<const void *>(tc_gemm_kernel<Cfg>);
     return k;
 }

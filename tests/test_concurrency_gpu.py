@@ -14,7 +14,7 @@ pytestmark = pytest.mark.gpu
 
 import software_pipelined_tiled_loop_gb300 as pg  # noqa: E402
 
-M, N, K = 1000, 1000, 4100  # stream-K halves for both tensor-core dtypes
+M, N, K = 1000, 1000, 4100  # stream-K halves (128 x 128 tiles) for both tensor-core dtypes
 
 
 @pytest.fixture(scope="module", autouse=True)

@@ -1,8 +1,11 @@
-"""Parity of the stream-K schedule of the persistent tensor-core kernels.
+"""Parity of the schedules of the leftover tiles of the persistent
+tensor-core kernels.
 
 The tiles a partial last wave would hold have their K-iterations dealt out
-to the resident slots; the pieces of a tile meet through global memory and
-the last to finish adds them.  These tests run shapes where the schedule
+to the resident slots (stream-K pieces); the pieces of a tile meet through
+global memory and the last to finish adds them.  Kernels with 256-wide
+tiles fed by TMA instead cut those tiles along N by default, into a left and
+a right half-width unit over all of K, which exchange nothing.  These tests run shapes where the schedule
 uses it (checked through pgemm_schedule first, so a test cannot pass by not
 splitting) and compare with the oracle: bit-exact for int8 and for
 integer-valued floats (a dropped, doubled or misplaced K range changes an
@@ -70,9 +73,9 @@ def check(orc, dtype, M, N, K, seed, kind="random", alpha=1, beta=0, config=None
 # 1000 x 1000 x 4100: fewer tiles than slots for every configuration, so every
 # element of C comes from stream-K pieces: with the cap at 8, 65 K-tiles in
 # ranges of 13 to 27, up to six pieces a tile, the last piece of a tile
-# ending on the ragged 65th K-tile; with the default cap, equal halves.
-# Bit-exact against the oracle on sampled entries and against the same call
-# without stream-K on all of C.
+# ending on the ragged 65th K-tile; with the default cap, equal halves (65
+# K-tiles: too many for half-width units).  Bit-exact against the oracle on
+# sampled entries and against the same call without stream-K on all of C.
 @pytest.mark.parametrize("dtype", ["bf16", "i8"])
 def test_every_config_stream_k_exactly(orc, dtype):
     M, N, K = 1000, 1000, 4100
@@ -92,7 +95,7 @@ def test_every_config_stream_k_exactly(orc, dtype):
         for cap in (0, 8):
             c = tuple(cfg) + (cap,)
             ok, s = splits(dtype, M, N, K, c)
-            assert ok and s["split_tiles"] == s["tiles"], (c, s)
+            assert ok and s["split_tiles"] == s["tiles"] and s["half_tiles"] == 0, (c, s)
             assert s["parts"] == 2 if cap == 0 else s["parts"] > 2, (c, s)
             got, status = run_gpu(dtype, A, B, C, one, zero, config=c)
             assert status == 0, (c, status)
@@ -171,12 +174,40 @@ def test_int8_exchange_stress(orc):
 
 
 def test_full_size_defaults_split():
-    """The bench's tensor-core workloads deal their leftover tiles out (on 152
-    SMs: 28 of int8 4096^3's 256 pair tiles, 36 of bf16 8192^3's 1024)."""
+    """The bench's tensor-core workloads deal their leftover tiles out along K
+    (on 152 SMs: 28 of int8 4096^3's 256 pair tiles, 36 of bf16 8192^3's
+    1024); with K of at most 32 K-tiles they cut them into half-width units."""
     for dtype, n in (("i8", 4096), ("bf16", 8192)):
         s = pg.pgemm_schedule(dtype, n, n, n)
         rem = s["tiles"] % s["slots"]
         assert rem > 0 and s["split_tiles"] == rem and 2 <= s["parts"] <= 8, s
+        assert s["half_tiles"] == 0, s
+    for dtype, K in (("bf16", 512), ("bf16", 2048), ("i8", 2048)):
+        s = pg.pgemm_schedule(dtype, 4096, 4096, K)
+        assert s["half_tiles"] == s["tiles"] % s["slots"] > 0 and s["split_tiles"] == 0, s
+
+
+# Half-width units (K of at most 32 K-tiles): bit-exact on integer-valued
+# operands against the oracle and the unsplit call, on shapes whose last tile
+# column is ragged (N = 1000: the right half of the last column partly beyond
+# N; N = 320: entirely beyond), with beta != 0 (only the computed half's
+# columns read C) and a ragged last K-tile.
+@pytest.mark.parametrize("dtype", ["bf16", "i8"])
+@pytest.mark.parametrize("M,N,K", [(1000, 1000, 2000), (700, 320, 1000), (2560, 2560, 1984)])
+@pytest.mark.parametrize("cfg", [(256, 256, 64, 6), (256, 256, 64, 4), (128, 256, 64, 4)])
+def test_half_width_units(orc, dtype, M, N, K, cfg):
+    if dtype == "i8" and cfg[0] == 128:
+        cfg = (128, 256, 64, 4)
+    s = pg.pgemm_schedule(dtype, M, N, K, cfg)
+    assert s["half_tiles"] > 0 and s["split_tiles"] == 0, s
+    one = 1 if dtype == "i8" else 1.0
+    beta = 3 if dtype == "i8" else 0.5
+    A, B, C = operands(dtype, M, N, K, si.config_seed(27, M + N + cfg[3]), "int")
+    got = check(orc, dtype, M, N, K, si.config_seed(27, M + N + cfg[3]), kind="int", alpha=one,
+                beta=beta, config=cfg)
+    plain, status = run_gpu(dtype, A, B, C, one, beta, config=tuple(cfg) + (1,))
+    assert status == 0
+    assert np.array_equal(got, plain)
 
 
 def test_scratch_pool_trim_and_reuse(orc):
