@@ -43,10 +43,11 @@ static KernelInfo info_i8() {
 
 // The staged producer on the CTA pair: `stages` names the depth of the int8
 // ring (the one that covers the memory latency); the fp16 ring behind it is
-// F16 deep (it only covers the widening); two transform groups.
+// F16 deep (it only covers the widening); two transform groups taking
+// alternate K-tiles where the ring depth is even, else one.
 template <int S8, int F16>
 static KernelInfo info_i8_staged() {
-    KernelInfo k = info_i8<256, F16, 2, 2, S8, 2>();
+    KernelInfo k = info_i8<256, F16, 2, 2, S8, S8 % 2 == 0 ? 2 : 1>();
     k.stages = S8;
     return k;
 }

@@ -109,3 +109,26 @@ def test_equals_tma_pair_full_size():
     b, sb = run_gpu("i8", A, B, C, 1, 0, config=(256, 256, 64, 6))
     assert sa == 0 and sb == 0
     assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("stages", [4, 5, 6])
+def test_back_to_back_calls(orc, stages):
+    """Many calls in a row on one stream, each checked bit for bit: a stage
+    widened before its copy had landed, or a ring whose phases slipped, would
+    show as wrong entries here."""
+    M, N, K = 1024, 1024, 4096
+    A, B, C = operands(M, N, K, 5400 + stages)
+    ref = torch.from_numpy(orc.gemm("i8", A, B, C, 1, 0).astype(np.int32)).cuda()
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    outs = [torch.empty((M, N), dtype=torch.int32, device="cuda") for _ in range(4)]
+    bad = 0
+    for i in range(60):
+        out = outs[i % 4]
+        out.fill_(-1)
+        pg.gemm_i8_ex(M, N, K, 1, dA, dB, 0, out, config=cfg(stages))
+        if i % 4 == 3:
+            torch.cuda.synchronize()
+            bad += sum(int((o != ref).sum().item()) for o in outs)
+    torch.cuda.synchronize()
+    assert pg.pgemm_get_device_status() == 0
+    assert bad == 0, f"{bad} wrong entries over 60 calls"
