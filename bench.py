@@ -183,9 +183,9 @@ def traffic_for(kernel_key: str):
 
 def launches_per_call(dtype: str, M: int, N: int, K: int) -> int:
     """This library's kernel launches in one default call: the operand pre-pass
-    (int8 widening of A and B in one launch; a repack per bf16/fp32 operand
-    whose pitch is not a multiple of 16 bytes), then the GEMM, which for fp32
-    is two grids when the stream-K tail is in use."""
+    (int8 widening of A and B in one launch; one launch repacking every
+    bf16/fp32 operand whose pitch is not a multiple of 16 bytes), then the
+    GEMM, which for fp32 is two grids when the stream-K tail is in use."""
     import software_pipelined_tiled_loop_gb300 as pg
     eb = {"f32": 4, "bf16": 2, "i8": 1}[dtype]
     n = 0
@@ -193,7 +193,7 @@ def launches_per_call(dtype: str, M: int, N: int, K: int) -> int:
         if dtype == "i8":
             n += 1
         else:
-            n += int((K * eb) % 16 != 0) + int((N * eb) % 16 != 0)
+            n += int((K * eb) % 16 != 0 or (N * eb) % 16 != 0)
     s = pg.pgemm_schedule(dtype, M, N, K)
     if dtype == "f32" and s["split_tiles"] > 0:
         n += 1 + int(s["tiles"] > s["split_tiles"])

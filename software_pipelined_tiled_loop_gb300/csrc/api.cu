@@ -299,8 +299,21 @@ __device__ __forceinline__ uint4 shift_bytes(uint4 lo, uint4 hi, uint32_t off) {
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-__global__ void repack_rows_kernel(const uint8_t *__restrict__ src, long long sld, uint8_t *__restrict__ dst,
-                                   long long dld, int rows, int cols, int eb) {
+struct RepackJob {
+    const uint8_t *src;
+    long long sld;
+    uint8_t *dst;
+    long long dld;
+    int rows, cols;
+};
+
+// blockIdx.y selects the operand: both repacks of a call in one launch.
+__global__ void repack_rows_kernel(RepackJob j0, RepackJob j1, int eb) {
+    const RepackJob &j = blockIdx.y == 0 ? j0 : j1;
+    const uint8_t *__restrict__ src = j.src;
+    uint8_t *__restrict__ dst = j.dst;
+    const long long sld = j.sld, dld = j.dld;
+    const int rows = j.rows, cols = j.cols;
     const long long row_bytes = static_cast<long long>(cols) * eb;
     const uint8_t *src_end = src + (static_cast<long long>(rows - 1) * sld + cols) * eb;
     for (int r = blockIdx.x; r < rows; r += gridDim.x) {
@@ -327,12 +340,24 @@ __global__ void repack_rows_kernel(const uint8_t *__restrict__ src, long long sl
     grid_launch_dependents();  // this block's rows are written
 }
 
-static cudaError_t launch_repack(const void *src, long long sld, void *dst, long long dld,
-                                 int rows, int cols, int eb, int sm_count, cudaStream_t s) {
-    if (rows <= 0 || cols <= 0) return cudaSuccess;
-    const int blocks = rows < sm_count * 8 ? rows : sm_count * 8;
-    repack_rows_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint8_t *>(src), sld,
-                                              static_cast<uint8_t *>(dst), dld, rows, cols, eb);
+// Repack one or two operands (rows = 0: none) in a single launch.
+static cudaError_t launch_repack(const void *src0, long long sld0, void *dst0, long long dld0,
+                                 int rows0, int cols0, const void *src1, long long sld1,
+                                 void *dst1, long long dld1, int rows1, int cols1, int eb,
+                                 int sm_count, cudaStream_t s) {
+    if (cols0 <= 0) rows0 = 0;
+    if (cols1 <= 0) rows1 = 0;
+    const RepackJob j0{static_cast<const uint8_t *>(src0), sld0, static_cast<uint8_t *>(dst0),
+                       dld0, rows0, cols0};
+    const RepackJob j1{static_cast<const uint8_t *>(src1), sld1, static_cast<uint8_t *>(dst1),
+                       dld1, rows1, cols1};
+    // operand 0 only, operand 1 only (as y = 0), or both
+    const RepackJob &a = rows0 > 0 ? j0 : j1;
+    const int ny = (rows0 > 0 && rows1 > 0) ? 2 : ((rows0 > 0 || rows1 > 0) ? 1 : 0);
+    if (ny == 0) return cudaSuccess;
+    const int most = rows0 > rows1 ? rows0 : rows1;
+    const int blocks = most < sm_count * 8 ? most : sm_count * 8;
+    repack_rows_kernel<<<dim3(blocks, ny), 256, 0, s>>>(a, j1, eb);
     return cudaGetLastError();
 }
 
@@ -491,13 +516,9 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
                                                 sched.counters,
                                                 static_cast<int>(sched.counter_words),
                                                 d->sm_count, stream);
-                cudaError_t e = cudaSuccess;
-                if (a_repack)
-                    e = launch_repack(A, lda, base, a_ld2, M, K, in_bytes, d->sm_count, stream);
-                if (e == cudaSuccess && b_repack)
-                    e = launch_repack(B, ldb, base + a_bytes, b_ld2, K, N, in_bytes, d->sm_count,
-                                      stream);
-                return e;
+                return launch_repack(A, lda, base, a_ld2, a_repack ? M : 0, K, B, ldb,
+                                     base + a_bytes, b_ld2, b_repack ? K : 0, N, in_bytes,
+                                     d->sm_count, stream);
             };
             if (a_repack) {
                 a_op = base;
