@@ -169,11 +169,13 @@ static const KernelInfo *table_of(pgemm_dtype dt, int *count) {
 //    stages drop to one block per SM and lose 16 %); 128 x 64 tiles when the
 //    128 x 128 grid would leave SMs without two blocks each.
 //  * bf16 and int8: 256 x 256 tiles on a CTA pair (cta_group::2) with six
-//    stages when the pairs cover the GPU (bf16 8192^3 +12 %, int8 4096^3
-//    +10 % over 128 x 256); else 128 x 256 with four stages when those tiles
-//    cover every SM; else 128 x 128.  At most two K-tiles (K <= 128): the call
-//    is bound by writing C, and 128 x 128 tiles with four stages (room for two
-//    epilogue staging buffers per warp) write it fastest.
+//    stages when the pairs cover half the SMs (bf16 8192^3 +12 %, int8
+//    4096^3 +10 % over 128 x 256); else 128 x 128.  (128 x 256 tiles never
+//    win the choice: a grid has at most twice as many of them as pair
+//    tiles, so whenever they would cover every SM the pairs cover half.)  At
+//    most two K-tiles (K <= 128): the call is bound by writing C, and 128 x
+//    128 tiles with four stages (room for two epilogue staging buffers per
+//    warp) write it fastest.
 static pgemm_config default_config(pgemm_dtype dt, int M, int N, int K, int sm_count) {
     pgemm_config c{128, 128, 0, 4};
     if (dt == PGEMM_F32) {
@@ -182,15 +184,12 @@ static pgemm_config default_config(pgemm_dtype dt, int M, int N, int K, int sm_c
         c.stages = 3;
         return c;
     }
-    const long long tiles256 = (long long)((M + 127) / 128) * ((N + 255) / 256);
     const long long pairs = (long long)((M + 255) / 256) * ((N + 255) / 256);
     if (K <= 128) return c;  // 128 x 128, four stages
     if (pairs >= sm_count / 2) {
         c.bm = 256;
         c.bn = 256;
         c.stages = 6;
-    } else if (tiles256 >= sm_count) {
-        c.bn = 256;
     }
     return c;
 }
@@ -557,6 +556,15 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
     }
     if (st != PGEMM_OK) return st;
 
+    // The in-kernel widening reads the caller's int8 operands by TMA.
+    alignas(64) CUtensorMap ta8, tb8;
+    if (fused && K > 0) {
+        st = encode_2d(&ta8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, A, K, M, lda, 64, 128, false);
+        if (st == PGEMM_OK)
+            st = encode_2d(&tb8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, N, K, ldb, 128, 64, false);
+        if (st != PGEMM_OK) return st;
+    }
+
     // C as a tensor map (32 x 32 boxes, 128-byte swizzle) when its rows are
     // 16-byte aligned, so that the tensor-core epilogue can store by TMA.
     alignas(64) CUtensorMap tc_map;
@@ -599,6 +607,8 @@ static pgemm_status gemm_impl(int M, int N, int K, Sc alpha, const In *A, const 
         p.a_ptr = a_op; p.b_ptr = b_op; p.lda = a_ld; p.ldb = b_ld;
         p.widen_src_a = A; p.widen_src_b = B; p.widen_lda = lda; p.widen_ldb = ldb;
         p.widen_ready = chunk_ready;
+        p.tmap_a8 = (fused && K > 0) ? &ta8 : nullptr;
+        p.tmap_b8 = (fused && K > 0) ? &tb8 : nullptr;
         p.after_prepass = after_prepass;
         p.sched = sched;
         p.alpha = alpha; p.beta = beta; p.C = C;

@@ -50,6 +50,9 @@ struct LaunchCommon {
     const CUtensorMap *tmap_a;
     const CUtensorMap *tmap_b;
     const CUtensorMap *tmap_c;  // C as a 32 x 32-box, 128-byte-swizzled map, or nullptr
+    // in-kernel widening: the caller's int8 A (128 x 64-byte boxes) and B
+    // (64 x 128-byte boxes), unswizzled; nullptr otherwise
+    const CUtensorMap *tmap_a8, *tmap_b8;
     bool after_prepass;         // a widening / repack kernel of this call precedes the GEMM
     KernelCtx ctx;
     TileSchedule sched;         // persistent kernels only

@@ -100,17 +100,22 @@ struct TcCfg {
     static constexpr int B_BYTES = B_COLS * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // per CTA
     static constexpr int TX_BYTES = STAGE_BYTES * CG;      // counted on the MMA's full barrier
-    // a half-width unit (BN = 256 tiles: columns [128 h, 128 h + 128) only)
+    // a half-width unit (BN = 256 tiles: columns [128 h, 128 h + 128) only).
+    // Not in the exact-int8 kernels: their epilogue holds 128 sums a thread,
+    // and the half-width bookkeeping beside them raised the default int8
+    // kernel's spills from 20 to 228 bytes of loads.
     static constexpr int STAGE_BYTES_HALF = A_BYTES + B_BYTES / 2;
     static constexpr int TX_BYTES_HALF = STAGE_BYTES_HALF * CG;
-    static constexpr bool HALVES = BN_ == 256 && (PROD_ == 0 || PROD_ == 3);
+    static constexpr bool HALVES = BN_ == 256 && !INT_FOLD_ && PROD_ == 0;
     // PROD = 2: the int8 staging ring (A 128 x 64 bytes, then B as B_COLS/64
     // boxes of 64 k-rows x 64 bytes; 64-byte rows, unswizzled).
-    static constexpr int S8 = PROD_ == 2 ? S8_ : 0;
+    // PROD = 3: the same ring holds the int8 boxes the widening warps convert
+    // (four slots of 8 KB)
+    static constexpr int S8 = PROD_ == 2 ? S8_ : (PROD_ == 3 ? 4 : 0);
     static constexpr int XG = PROD_ == 2 ? XG_ : 1;        // transform groups
     static constexpr int XG_WARPS = 4 / XG;                // warps per transform group
     static constexpr int A8_BYTES = BM * BK;               // int8
-    static constexpr int STAGE8_BYTES = (BM + B_COLS) * BK;
+    static constexpr int STAGE8_BYTES = PROD_ == 3 ? 8192 : (BM + B_COLS) * BK;
     static constexpr int RING8_BYTES = S8 * STAGE8_BYTES;
     // Epilogue staging: one or two 32x32 fp32 blocks per epilogue warp (two
     // let a TMA store drain while the next block is staged), as many as fit.
@@ -132,7 +137,6 @@ struct TcCfg {
     static constexpr int FULL_ARRIVALS = PROD == 1 ? 4 * CG : (PROD == 2 ? XG_WARPS * CG : 1);
     // setmaxnreg shares of the PROD = 1 layout (launched at 65536 / THREADS)
     static constexpr int REGS_PRODUCER = 104, REGS_MMA = 48, REGS_EPILOGUE = 176;
-    static constexpr int WIDEN_DEPTH = 6;  // PROD = 3: widening steps in flight per thread
     static constexpr int WIDEN_CHUNK = 256; // PROD = 3: K chunk (elements) published at once
     static constexpr int RING8_OFFSET = STAGES * STAGE_BYTES;
     static constexpr int STAGING_OFFSET = RING8_OFFSET + RING8_BYTES;
@@ -476,105 +480,74 @@ struct TcOperands {
     uint32_t *ready;  // one per 64-wide K chunk, zero at launch
 };
 
-// In-kernel widening (PROD = 3), run by the 128 threads of warps 0-3 of
-// every CTA (global widening thread g of T = 128 * gridDim.x).  K chunk c is
-// A's columns [KW c, KW c + KW) and B's rows [KW c, KW c + KW), cut into
-// 16-byte pieces: A's M rows of w/16 pieces each, then B's w rows of N/16
-// pieces (w = the chunk's width, KW but for a narrower last chunk; K and N
-// are multiples of 16).  Each step a thread widens two pieces, g + (2 sub + j) T
-// for j = 0, 1, of the chunk's ceil(pieces / 2T) steps, so all lanes of a
-// warp finish a chunk together: the warp then fences and adds one to the
-// chunk's counter (release, GPU scope).  The chunk is complete when the
-// counter reaches 4 * gridDim.x.  Steps are software-pipelined D deep: the
-// loads of step s + D - 1 are issued before step s is converted and stored,
-// so that D steps of loads are in flight per thread.  Consecutive lanes take
-// consecutive pieces: a warp reads 64-byte row segments of A (or 512
-// contiguous bytes of B) and writes whole 128-byte lines.
-template <int D, int KW>
-__device__ __forceinline__ void fused_widen(const TcOperands &op, int M, int N, int K,
-                                            uint32_t g, uint32_t T) {
-    const int nchunks = (K + KW - 1) / KW;
-    if (nchunks == 0) return;
-    const long long npb = N / 16;  // pieces per B row
-    const int w_last = K - (nchunks - 1) * KW;
-    const long long TT = 2LL * T;
-    const long long p_full = (KW / 16LL) * M + KW * npb;
-    const long long p_last = static_cast<long long>(w_last / 16) * M + w_last * npb;
-    const int spc_full = static_cast<int>((p_full + TT - 1) / TT);
-    const int spc_last = static_cast<int>((p_last + TT - 1) / TT);
-    const int nsteps = (nchunks - 1) * spc_full + spc_last;
-    // step s -> (chunk, step within the chunk)
-    auto locate = [&](int s, int &c, int &sub) {
-        c = s < (nchunks - 1) * spc_full ? s / spc_full : nchunks - 1;
-        sub = s - c * spc_full;
-    };
-    // piece j of step s: source and destination, or false if past the chunk
-    auto piece = [&](int c, int sub, int j, const int8_t *&src, __half *&dst) -> bool {
-        const bool last = c == nchunks - 1;
-        const long long pa = last ? w_last / 16 : KW / 16;
-        const long long rows_b = last ? w_last : KW;
-        const long long i = g + (2LL * sub + j) * T;
-        if (i < pa * M) {
-            const long long r = i / pa, q = i - r * pa;
-            src = op.A + r * op.lda + static_cast<long long>(KW) * c + 16 * q;
-            dst = op.A16 + r * op.lda16 + static_cast<long long>(KW) * c + 16 * q;
-            return true;
+// In-kernel widening (PROD = 3).  K chunk c is A's columns [KW c, KW c + KW)
+// and B's rows [KW c, KW c + KW) (KW = WIDEN_CHUNK, the last chunk possibly
+// narrower), cut into 8 KB int8 boxes: A boxes of 128 rows x 64 columns
+// (bytes), then B boxes of 64 rows x 128 columns.  The boxes of a chunk are
+// dealt to the CTAs round-robin (box b to CTA b mod G); every CTA walks its
+// boxes chunk by chunk.  One lane TMA-loads them into a four-slot int8 ring;
+// the 128 threads of warps 0-3 convert each landed box to fp16 and store it
+// into the fp16 copies (thread t: 16-byte pieces t, t + 128, ... of the box,
+// so a warp reads 512 consecutive bytes of the box and writes whole 128-byte
+// lines), release the slot, and after their last box of a chunk publish it:
+// a fence (the thread's own stores; no load of the thread is in flight, the
+// copies being the TMA's), then a release add on the chunk's counter by each
+// warp.  The chunk is complete at 4 * gridDim.x.
+struct WidenBoxes {
+    int M, N, K, KW, nchunks, mb, nb;  // row blocks of A (128), column blocks of B (128)
+
+    __device__ __forceinline__ WidenBoxes(int M_, int N_, int K_, int KW_)
+        : M(M_), N(N_), K(K_), KW(KW_), nchunks((K_ + KW_ - 1) / KW_), mb((M_ + 127) / 128),
+          nb((N_ + 127) / 128) {}
+    // 64-wide K blocks of chunk c
+    __device__ __forceinline__ int kblocks(int c) const {
+        const int w = min(KW, K - c * KW);
+        return (w + 63) / 64;
+    }
+    __device__ __forceinline__ int boxes(int c) const { return kblocks(c) * (mb + nb); }
+    // box b of chunk c: operand (A or B) and the box's origin
+    __device__ __forceinline__ void decode(int c, int b, bool &is_a, int &x, int &y) const {
+        const int na = kblocks(c) * mb;
+        is_a = b < na;
+        if (is_a) {  // A: x = K column (bytes), y = row
+            x = c * KW + (b % kblocks(c)) * 64;
+            y = (b / kblocks(c)) * 128;
+        } else {     // B: x = N column, y = K row
+            const int bb = b - na;
+            x = (bb % nb) * 128;
+            y = c * KW + (bb / nb) * 64;
         }
-        const long long i2 = i - pa * M;
-        if (i2 >= rows_b * npb) return false;
-        const long long rb = i2 / npb, q = i2 - rb * npb;
-        const long long r = static_cast<long long>(KW) * c + rb;
-        src = op.B + r * op.ldb + 16 * q;
-        dst = op.B16 + r * op.ldb16 + 16 * q;
-        return true;
-    };
-    auto load = [&](int s, uint4 (&v)[2]) {
-        int c, sub;
-        locate(s, c, sub);
+    }
+};
+
+// Convert one landed 8 KB int8 box in shared memory (`box`) to fp16 in the
+// destination copy, skipping the pieces beyond the matrix (K and N are
+// multiples of 16, so every 16-byte piece is wholly inside or outside).
+__device__ __forceinline__ void widen_box(const TcOperands &op, const WidenBoxes &wb, bool is_a,
+                                          int x, int y, uint32_t box, uint32_t t) {
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int8_t *src;
-            __half *dst;
-            v[j] = make_uint4(0u, 0u, 0u, 0u);
-            if (piece(c, sub, j, src, dst)) v[j] = ldg_nc_v4(src);
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t p = t + 128u * j;  // 16-byte piece of the box
+        int r, cx;                        // row and column (bytes) of the piece in the matrix
+        const int8_t *unused = nullptr;
+        (void)unused;
+        if (is_a) {  // 128 rows of 64 bytes: 4 pieces a row
+            r = y + static_cast<int>(p >> 2);
+            cx = x + static_cast<int>(p & 3u) * 16;
+        } else {     // 64 rows of 128 bytes: 8 pieces a row
+            r = y + static_cast<int>(p >> 3);
+            cx = x + static_cast<int>(p & 7u) * 16;
         }
-    };
-    auto store = [&](int s, const uint4 (&v)[2]) {
-        int c, sub;
-        locate(s, c, sub);
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int8_t *src;
-            __half *dst;
-            if (piece(c, sub, j, src, dst)) {
-                uint32_t o[8];
-                widen16(v[j], o);
-                uint4 *d = reinterpret_cast<uint4 *>(dst);
-                d[0] = make_uint4(o[0], o[1], o[2], o[3]);
-                d[1] = make_uint4(o[4], o[5], o[6], o[7]);
-            }
-        }
-        if (sub == (c == nchunks - 1 ? spc_last : spc_full) - 1) {
-            // this warp's share of chunk c is written: publish it
-            __threadfence();
-            fence_proxy_async_global();
-            __syncwarp();
-            if ((threadIdx.x & 31u) == 0) red_release_add(op.ready + c, 1u);
-        }
-    };
-    uint4 x[D][2];
-#pragma unroll
-    for (int d = 0; d < D - 1; ++d)
-        if (d < nsteps) load(d, x[d]);
-    for (int s0 = 0; s0 < nsteps; s0 += D) {
-#pragma unroll
-        for (int d = 0; d < D; ++d) {
-            const int s = s0 + d;
-            if (s < nsteps) {
-                if (s + D - 1 < nsteps) load(s + D - 1, x[(d + D - 1) % D]);
-                store(s, x[d]);
-            }
-        }
+        const uint4 v = lds_u4(box + p * 16);
+        const bool in = is_a ? (r < wb.M && cx < wb.K) : (r < wb.K && cx < wb.N);
+        if (!in) continue;
+        uint32_t o[8];
+        widen16(v, o);
+        __half *dst = is_a ? op.A16 + static_cast<long long>(r) * op.lda16 + cx
+                           : op.B16 + static_cast<long long>(r) * op.ldb16 + cx;
+        uint4 *d = reinterpret_cast<uint4 *>(dst);
+        d[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        d[1] = make_uint4(o[4], o[5], o[6], o[7]);
     }
 }
 
@@ -696,6 +669,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b,
                    const __grid_constant__ CUtensorMap tmap_c,
+                   const __grid_constant__ CUtensorMap tmap_a8,
+                   const __grid_constant__ CUtensorMap tmap_b8,
                    const GemmArgs<typename Cfg::Scalar, typename Cfg::Scalar> args,
                    const TcOperands ops, const KernelCtx ctx) {
     using Scalar = typename Cfg::Scalar;
@@ -730,6 +705,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             prefetch_tmap(&tmap_b);
         }
         if (args.c_tma) prefetch_tmap(&tmap_c);
+        if constexpr (Cfg::PROD == 3) {
+            prefetch_tmap(&tmap_a8);
+            prefetch_tmap(&tmap_b8);
+        }
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], Cfg::FULL_ARRIVALS);
             // released by the MMA issuer (with a CTA pair: the even CTA's, whose
@@ -746,6 +725,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             mbar_init(&full8[s], 1);                 // the int8 producer's expect_tx
             mbar_init(&empty8[s], Cfg::XG_WARPS);    // the warps of the group that widens it
         }
+        // (PROD = 3: XG_WARPS = 4, the four widening warps release each box)
         fence_barrier_init();
     }
     if (warp == Cfg::MMA_WARP) {
@@ -832,9 +812,33 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         if constexpr (Cfg::PROD == 3) {
             // ------- the widening pass, inside the GEMM (warps 0-3) -------
             setmaxnreg_dec<Cfg::REGS_PRODUCER>();
-            fused_widen<Cfg::WIDEN_DEPTH, Cfg::WIDEN_CHUNK>(ops, args.M, args.N, args.K,
-                                                            blockIdx.x * 128u + threadIdx.x,
-                                                            gridDim.x * 128u);
+            const WidenBoxes wb(args.M, args.N, args.K, Cfg::WIDEN_CHUNK);
+            const int G = static_cast<int>(gridDim.x);
+            uint32_t it = 0;  // this CTA's boxes so far (ring position)
+            bool ok = true;
+            for (int c = 0; c < wb.nchunks; ++c) {
+                const int nbx = wb.boxes(c);
+                for (int b = static_cast<int>(blockIdx.x); ok && b < nbx; b += G, ++it) {
+                    const uint32_t s8 = it % Cfg::S8, ph8 = (it / Cfg::S8) & 1u;
+                    if (!mbar_wait(&full8[s8], ph8, ctx, kSiteConvertFull)) {
+                        ok = false;
+                        break;
+                    }
+                    bool is_a;
+                    int x, y;
+                    wb.decode(c, b, is_a, x, y);
+                    widen_box(ops, wb, is_a, x, y, smem_u32(sRing8 + s8 * Cfg::STAGE8_BYTES),
+                              threadIdx.x);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty8[s8]);  // the box has been read
+                }
+                if (!ok) break;
+                // this warp's share of chunk c is written: publish it
+                __threadfence();
+                fence_proxy_async_global();
+                __syncwarp();
+                if (lane == 0) red_release_add(ops.ready + c, 1u);
+            }
         } else if constexpr (Cfg::PROD == 2) {
             // ------- int8 stages widened into fp16 stages (warps 0-3) -------
             // Group g of XG takes the slot's K-tiles g, g + XG, ...  For each:
@@ -987,6 +991,29 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     } else if (Cfg::PROD ? warp >= static_cast<uint32_t>(Cfg::MMA_WARP) : warp == 1) {
         if constexpr (Cfg::PROD) setmaxnreg_dec<Cfg::REGS_MMA>();  // the MMA warpgroup
         if constexpr (Cfg::PROD == 3) {
+            if (warp == Cfg::TMA8_WARP + 1 && lane == 0) {
+                // ------- the widening's int8 boxes by TMA into the int8 ring -------
+                const WidenBoxes wb(args.M, args.N, args.K, Cfg::WIDEN_CHUNK);
+                const int G = static_cast<int>(gridDim.x);
+                uint32_t it = 0;
+                bool ok = true;
+                for (int c = 0; ok && c < wb.nchunks; ++c) {
+                    const int nbx = wb.boxes(c);
+                    for (int b = static_cast<int>(blockIdx.x); b < nbx; b += G, ++it) {
+                        const uint32_t s8 = it % Cfg::S8, ph8 = (it / Cfg::S8) & 1u;
+                        if (!mbar_wait(&empty8[s8], ph8 ^ 1u, ctx, kSiteProducerEmpty)) {
+                            ok = false;
+                            break;
+                        }
+                        bool is_a;
+                        int x, y;
+                        wb.decode(c, b, is_a, x, y);
+                        mbar_arrive_expect_tx(&full8[s8], Cfg::STAGE8_BYTES);
+                        tma_load_2d(sRing8 + s8 * Cfg::STAGE8_BYTES, is_a ? &tmap_a8 : &tmap_b8,
+                                    &full8[s8], x, y);
+                    }
+                }
+            }
             if (warp == Cfg::TMA8_WARP && lane == 0) {
                 // K chunks complete in order for every warp that widens, so
                 // chunk kt complete means every chunk before it is too
@@ -1385,7 +1412,11 @@ static cudaError_t launch_tc(const P &p, cudaStream_t stream) {
         ops.lda = p.lda;
         ops.ldb = p.ldb;
     }
-    return cudaLaunchKernelEx(&lc, tc_gemm_kernel<Cfg>, *p.tmap_a, *p.tmap_b, tc, a, ops, p.ctx);
+    // the widening's int8 maps (PROD = 3); any valid map for the others
+    const CUtensorMap &ta8 = p.tmap_a8 != nullptr ? *p.tmap_a8 : *p.tmap_a;
+    const CUtensorMap &tb8 = p.tmap_b8 != nullptr ? *p.tmap_b8 : *p.tmap_b;
+    return cudaLaunchKernelEx(&lc, tc_gemm_kernel<Cfg>, *p.tmap_a, *p.tmap_b, tc, ta8, tb8, a, ops,
+                              p.ctx);
 }
 
 // Schedule slots of a persistent launch: resident CTAs (at most MAX_BLOCKS per

@@ -74,7 +74,7 @@ def test_list_configs(L):
     assert not [c for c in f32 + bf16 if len(c) > 5 and c[5] == pg.PRODUCERS["staged"]]
     # int8 on the CTA pair with the widening inside the GEMM
     i8_wik = [c for c in i8 if len(c) > 5 and c[5] == pg.PRODUCERS["widen_in_kernel"]]
-    assert {(c[0], c[1], c[3]) for c in i8_wik} == {(256, 256, 5), (256, 256, 6)}
+    assert {(c[0], c[1], c[3]) for c in i8_wik} == {(256, 256, 4), (256, 256, 5)}
     # the mma.sync int8 engine: 128 x 128 tiles, K-tiles of 128 int8
     imma = [c for c in i8 if len(c) > 6 and c[6] == pg.ENGINES["mma_sync"]]
     assert {(c[0], c[1], c[2]) for c in imma} == {(128, 128, 128)}

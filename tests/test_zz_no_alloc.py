@@ -62,18 +62,18 @@ def _run(fn, M, N, K, alpha, beta, seed):
 # exactly, whatever the previous call left in the shared array.  The ragged
 # shape (K, N odd) exercises the rounded-up pitches of the widened operands;
 # 1024 x 1024 x 8192 is one that gemm_i8 splits along K (stream-K) while this
-# entry point, which has no memory for the exchange, does not; 2560 x 2560 x
-# 2048 is one whose leftover tiles both run as half-width units.
+# entry point, which has no memory for the exchange, does not; so does 2560 x
+# 2560 x 2048 on the CTA pair.
 RAGGED = (1001, 1003, 2005, 3, -2, 31)
 SPLIT = (1024, 1024, 8192, 1, 0, 41)
-HALVES = (2560, 2560, 2048, 2, 1, 43)
-CASES = [(1000, 1500, 2000, 1, 0, 11), (2048, 777, 3000, -3, 2, 23), RAGGED, SPLIT, HALVES,
+PAIR = (2560, 2560, 2048, 2, 1, 43)
+CASES = [(1000, 1500, 2000, 1, 0, 11), (2048, 777, 3000, -3, 2, 23), RAGGED, SPLIT, PAIR,
          (1000, 1500, 2000, 1, 0, 11)]
 
 
 def test_noalloc_matches_gemm_i8_on_consecutive_calls():
     assert pg.pgemm_schedule("i8", *SPLIT[:3])["split_tiles"] > 0  # gemm_i8 splits this one
-    assert pg.pgemm_schedule("i8", *HALVES[:3])["half_tiles"] > 0
+    assert pg.pgemm_schedule("i8", *PAIR[:3])["split_tiles"] > 0
     for (M, N, K, alpha, beta, seed) in CASES:
         assert scratch_needed(M, N, K) <= LIMIT
         want = _run(pg.gemm_i8, M, N, K, alpha, beta, seed)
