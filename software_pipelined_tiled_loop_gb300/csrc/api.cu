@@ -168,9 +168,13 @@ static const KernelInfo *table_of(pgemm_dtype dt, int *count) {
 //  * fp32: 128 x 128 tiles with three stages (two blocks per SM; four or more
 //    stages drop to one block per SM and lose 16 %); 128 x 64 tiles when the
 //    128 x 128 grid would leave SMs without two blocks each.
-//  * bf16 and int8: 256 x 256 tiles on a CTA pair (cta_group::2) with six
-//    stages when the pairs cover half the SMs (bf16 8192^3 +12 %, int8
-//    4096^3 +10 % over 128 x 256); else 128 x 128.  (128 x 256 tiles never
+//  * bf16 and int8: 256 x 256 tiles on a CTA pair (cta_group::2) when the
+//    pairs cover half the SMs (bf16 8192^3 +12 %, int8 4096^3 +10 % over
+//    128 x 256), with three stages of 128 K columns, each landed as two
+//    64-column sub-tiles under one barrier: the MMA warp then waits, commits
+//    and loops once per 8 MMAs instead of 4 (against six 64-column stages in
+//    the same shared memory: bf16 4096^2 x 512 -8 %, x 2048 -4 %, 8192^3
+//    -1 %, int8 4096^3 -1 %); else 128 x 128.  (128 x 256 tiles never
 //    win the choice: a grid has at most twice as many of them as pair
 //    tiles, so whenever they would cover every SM the pairs cover half.)  At
 //    most two K-tiles (K <= 128): the call is bound by writing C, and 128 x
@@ -189,7 +193,8 @@ static pgemm_config default_config(pgemm_dtype dt, int M, int N, int K, int sm_c
     if (pairs >= sm_count / 2) {
         c.bm = 256;
         c.bn = 256;
-        c.stages = 6;
+        c.bk = 128;
+        c.stages = 3;
     }
     return c;
 }
@@ -211,18 +216,19 @@ static pgemm_config default_config(pgemm_dtype dt, int M, int N, int K, int sm_c
 constexpr int kTcMaxPieces = 2;
 
 // Half-width units instead (kernels with 256-wide tiles fed by TMA, the
-// library's default up to kHalvesMaxKTiles K-tiles): when the R leftover
+// library's default up to kHalvesMaxK K columns): when the R leftover
 // tiles fit twice on the slots, each is cut along N into its left and right
 // 128 columns, 2R units of the full K range that exchange nothing (no
 // partial-sum memory, no counters), so the wave after them is never held up
-// by an exchange.  A half-width unit's N = 128 MMAs read A in full for half
+// by an exchange.  The limit is in K columns (kHalvesMaxK), whatever the
+// kernel's K-tile width.  A half-width unit's N = 128 MMAs read A in full for half
 // the products, so per K-tile it costs more than half a whole tile; with
 // long K that outweighs the exchange it saves (bf16 4096^2: K = 512 24.6
 // against 26.6 us without a split, K = 2048 53.2 against 55.9 us with K
 // halves; K = 16384 328.7 against 311.8 us, and int8 4096^3 108.8 against
 // 106.2 us).  An explicit max_k_parts > 1 asks for stream-K pieces.
 // allow_k_split = false: a call that may not allocate (no exchange memory).
-constexpr int kHalvesMaxKTiles = 32;
+constexpr int kHalvesMaxK = 2048;
 static TileSchedule plan_schedule(const KernelInfo &k, int M, int N, int K, int slots,
                                   int max_parts, bool allow_k_split = true) {
     TileSchedule s;
@@ -230,7 +236,7 @@ static TileSchedule plan_schedule(const KernelInfo &k, int M, int N, int K, int 
     s.slots = slots;
     if (k.schedule_slots == nullptr) return s;
     const int T = (K + k.bk - 1) / k.bk;
-    if (k.halves && max_parts == 0 && T > 0 && T <= kHalvesMaxKTiles) {
+    if (k.halves && max_parts == 0 && K > 0 && K <= kHalvesMaxK) {
         const long long rem = s.tiles % slots;
         if (rem > 0 && 2 * rem <= slots) {
             s.half_tiles = rem;

@@ -12,14 +12,16 @@ namespace pg {
 // which leaves room for two resident blocks per SM.
 // CM = CG = 2: a CTA pair computes a 256 x BN tile with one M = 256 MMA (each
 // CTA holds half of A's rows and half of B's columns), listed as bm = 256.
-template <int BN, int STAGES, int CM = 1>
+// KSUB = 2: stages of 128 K columns (two 64-wide sub-tiles under one barrier
+// pair), listed as bk = 128.
+template <int BN, int STAGES, int CM = 1, int KSUB = 1>
 using Bf16Cfg = TcCfg<BN, STAGES, /*KC=*/0, /*BF16=*/1, /*INT_FOLD=*/false,
-                      (BN == 256 || STAGES >= 3) ? 8 : 4, CM, CM>;
+                      (BN == 256 || STAGES >= 3) ? 8 : 4, CM, CM, 0, 0, 1, KSUB>;
 
-template <int BN, int STAGES, int CM = 1>
+template <int BN, int STAGES, int CM = 1, int KSUB = 1>
 static KernelInfo info_bf16() {
-    KernelInfo k = tc_info<Bf16Cfg<BN, STAGES, CM>>();
-    k.launch_bf16 = launch_tc<Bf16Cfg<BN, STAGES, CM>, LaunchBf16>;
+    KernelInfo k = tc_info<Bf16Cfg<BN, STAGES, CM, KSUB>>();
+    k.launch_bf16 = launch_tc<Bf16Cfg<BN, STAGES, CM, KSUB>, LaunchBf16>;
     return k;
 }
 
@@ -32,6 +34,8 @@ const KernelInfo *bf16_kernels(int *count) {
         // comparator: "kernel 10" of the SGEMM page)
         info_bf16<256, 1>(), info_bf16<128, 1>(),
         info_bf16<256, 4, 2>(), info_bf16<256, 5, 2>(), info_bf16<256, 6, 2>(),
+        // the CTA pair with 128-column stages (three = the bytes of six 64-wide ones)
+        info_bf16<256, 2, 2, 2>(), info_bf16<256, 3, 2, 2>(),
     };
     *count = static_cast<int>(sizeof(table) / sizeof(table[0]));
     return table;

@@ -29,13 +29,14 @@ constexpr int kI8ChunkTiles = 16;  // 16 K-tiles of 64 = 1024 products per exact
 
 // Each epilogue thread keeps a 128-column row of int32 sums in registers:
 // 128-wide tiles use four epilogue warps, 256-wide tiles eight.
-template <int BN, int STAGES, int CM = 1, int PROD = 0, int S8 = 0, int XG = 1>
-using I8Cfg = TcCfg<BN, STAGES, kI8ChunkTiles, /*BF16=*/0, /*INT_FOLD=*/true, BN == 256 ? 8 : 4,
-                    CM, CM, PROD, S8, XG>;
+// KSUB = 2: stages of 128 K columns; a round is then 8 stages (1024 products).
+template <int BN, int STAGES, int CM = 1, int PROD = 0, int S8 = 0, int XG = 1, int KSUB = 1>
+using I8Cfg = TcCfg<BN, STAGES, kI8ChunkTiles / KSUB, /*BF16=*/0, /*INT_FOLD=*/true,
+                    BN == 256 ? 8 : 4, CM, CM, PROD, S8, XG, KSUB>;
 
-template <int BN, int STAGES, int CM = 1, int PROD = 0, int S8 = 0, int XG = 1>
+template <int BN, int STAGES, int CM = 1, int PROD = 0, int S8 = 0, int XG = 1, int KSUB = 1>
 static KernelInfo info_i8() {
-    using Cfg = I8Cfg<BN, STAGES, CM, PROD, S8, XG>;
+    using Cfg = I8Cfg<BN, STAGES, CM, PROD, S8, XG, KSUB>;
     KernelInfo k = tc_info<Cfg>();
     k.launch_i8 = launch_tc<Cfg, LaunchI8>;
     return k;
@@ -67,6 +68,8 @@ const KernelInfo *i8_kernels(int *count) {
             // CTA pair with the widening inside the GEMM (its int8 ring takes
             // the room of a sixth fp16 stage)
             info_i8<256, 4, 2, 3>(), info_i8<256, 5, 2, 3>(),
+            // the CTA pair with 128-column stages
+            info_i8<256, 2, 2, 0, 0, 1, 2>(), info_i8<256, 3, 2, 0, 0, 1, 2>(),
         };
         int n = 0;
         const KernelInfo *imma = i8_imma_kernels(&n);

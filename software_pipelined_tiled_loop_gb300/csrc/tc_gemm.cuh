@@ -85,10 +85,18 @@ namespace pg {
 // another, while one lane of warp 4 + EPI + 1 fills the ring by TMA from
 // those copies as in 0, waiting for each K chunk to be complete in every
 // CTA before it loads from it (FusedWiden).
+// KSUB: 64-wide K sub-tiles per stage (1 or 2).  With two, a stage holds
+// 128 K columns under one full / empty barrier pair and the MMA issuer issues
+// eight MMAs per wait and commit instead of four: the per-stage bookkeeping
+// of the issuer (barrier wait, commit, loop) is paid half as often.  The TMA
+// boxes and the shared-memory layout of each sub-tile are those of a
+// one-sub-tile stage.
 template <int BN_, int STAGES_, int KC_, int BF16_, bool INT_FOLD_, int EPI_ = 4, int CM_ = 1,
-          int CG_ = 1, int PROD_ = 0, int S8_ = 0, int XG_ = 1>
+          int CG_ = 1, int PROD_ = 0, int S8_ = 0, int XG_ = 1, int KSUB_ = 1>
 struct TcCfg {
     static constexpr int BM = 128, BN = BN_, BK = 64, STAGES = STAGES_, KC = KC_, CM = CM_;
+    static constexpr int KSUB = KSUB_;
+    static constexpr int SBK = BK * KSUB;  // K columns per stage (a "K-tile" of the schedule)
     static constexpr int CG = CG_;
     static constexpr int B_COLS = BN / CG;  // B columns this CTA loads and holds
     static constexpr int BF16 = BF16_;
@@ -96,8 +104,10 @@ struct TcCfg {
     static constexpr int EPI = EPI_;
     static constexpr int EPI_COLS = BN * 4 / EPI;  // columns per epilogue warp
     using Scalar = typename std::conditional<INT_FOLD, int32_t, float>::type;
-    static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = B_COLS * BK * 2;
+    static constexpr int A_SUB = BM * BK * 2;      // one 64-wide sub-tile of A
+    static constexpr int B_SUB = B_COLS * BK * 2;  // and of B
+    static constexpr int A_BYTES = A_SUB * KSUB;
+    static constexpr int B_BYTES = B_SUB * KSUB;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // per CTA
     static constexpr int TX_BYTES = STAGE_BYTES * CG;      // counted on the MMA's full barrier
     // a half-width unit (BN = 256 tiles: columns [128 h, 128 h + 128) only).
@@ -152,13 +162,15 @@ struct TcCfg {
     static_assert(EPI == 4 || EPI == 8, "EPI");
     static_assert(EPI_COLS % 32 == 0, "epilogue column split");
     static_assert(!INT_FOLD || EPI_COLS == 128, "the int32 fold keeps 128 columns per thread");
-    static_assert(!INT_FOLD || KC * BK <= 1024, "a round's fp32 sum must stay below 2^24");
+    static_assert(!INT_FOLD || KC * SBK <= 1024, "a round's fp32 sum must stay below 2^24");
+    static_assert(KSUB == 1 || (KSUB == 2 && (PROD_ == 0 || PROD_ == 3)),
+                  "two sub-tiles a stage: TMA-fed kernels only");
     static_assert(USED + 1024 <= 232448, "shared memory");
     static_assert((CM == 1 && CG == 1) || (CM == 2 && CG == 2 && (BN / 64) % 2 == 0),
                   "a CTA pair is a cluster of two splitting B's columns in halves");
     static_assert(!PROD || (INT_FOLD && EPI == 8 && B_COLS % 128 == 0),
                   "register-staged producer: int8 operands, two epilogue warpgroups");
-    static_assert(WIDEN_CHUNK % BK == 0, "a K chunk holds whole K-tiles");
+    static_assert(WIDEN_CHUNK % SBK == 0, "a K chunk holds whole K-tiles");
     static_assert(PROD != 2 || (S8 >= 2 && (XG == 1 || XG == 2) && B_COLS == 128),
                   "staged producer: an int8 ring of two or more stages, one or two groups");
     // Every use of an int8 slot must fall to the same transform group.  A
@@ -783,17 +795,26 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     const uint32_t full_lead = mapa_shared(smem_u32(&full[s]), 0);
                     if (crank == 0)
                         mbar_arrive_expect_tx(&full[s], hf ? Cfg::TX_BYTES_HALF : Cfg::TX_BYTES);
-                    tma_load_2d_pair(sA + s * Cfg::A_BYTES, &tmap_a, full_lead, kt * BK, m0);
-                    for (int j = 0; j < b_cols / 64; ++j)
-                        tma_load_2d_pair(sB + s * Cfg::B_BYTES + j * (BK * 128), &tmap_b,
-                                         full_lead, nb + j * 64, kt * BK);
+#pragma unroll
+                    for (int q = 0; q < Cfg::KSUB; ++q) {
+                        const int k0 = kt * Cfg::SBK + q * BK;
+                        tma_load_2d_pair(sA + s * Cfg::A_BYTES + q * Cfg::A_SUB, &tmap_a, full_lead,
+                                         k0, m0);
+                        for (int j = 0; j < b_cols / 64; ++j)
+                            tma_load_2d_pair(sB + s * Cfg::B_BYTES + q * Cfg::B_SUB + j * (BK * 128),
+                                             &tmap_b, full_lead, nb + j * 64, k0);
+                    }
                     continue;
                 }
                 mbar_arrive_expect_tx(&full[s], hf ? Cfg::STAGE_BYTES_HALF : Cfg::STAGE_BYTES);
-                tma_load_2d(sA + s * Cfg::A_BYTES, &tmap_a, &full[s], kt * BK, m0);
-                for (int j = 0; j < b_cols / 64; ++j)
-                    tma_load_2d(sB + s * Cfg::B_BYTES + j * (BK * 128), &tmap_b, &full[s],
-                                nb + j * 64, kt * BK);
+#pragma unroll
+                for (int q = 0; q < Cfg::KSUB; ++q) {
+                    const int k0 = kt * Cfg::SBK + q * BK;
+                    tma_load_2d(sA + s * Cfg::A_BYTES + q * Cfg::A_SUB, &tmap_a, &full[s], k0, m0);
+                    for (int j = 0; j < b_cols / 64; ++j)
+                        tma_load_2d(sB + s * Cfg::B_BYTES + q * Cfg::B_SUB + j * (BK * 128), &tmap_b,
+                                    &full[s], nb + j * 64, k0);
+                }
             }
         }
         if constexpr (Cfg::CM > 1) {
@@ -1020,7 +1041,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 int ready_upto = 0;
                 const uint32_t target = 4u * gridDim.x;
                 tma_producer([&](int kt) -> bool {
-                    const int c = kt * BK / Cfg::WIDEN_CHUNK;  // the K chunk holding K-tile kt
+                    const int c = kt * Cfg::SBK / Cfg::WIDEN_CHUNK;  // the K chunk holding K-tile kt
                     if (c < ready_upto) return true;
                     if (!wait_counter(ops.ready + c, target, ctx, kSiteWidenChunk)) return false;
                     fence_proxy_async_global();  // the TMA copies below read what was published
@@ -1098,17 +1119,24 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t a_addr = smem_u32(sA + s * Cfg::A_BYTES);
-                        const uint32_t b_addr = smem_u32(sB + s * Cfg::B_BYTES);
                         const bool first = kt == k_begin;
 #pragma unroll
-                        for (int k = 0; k < BK / 16; ++k) {
-                            const uint64_t ad = smem_desc_sw128(a_addr + k * 32, 16, 1024);
-                            const uint64_t bd = smem_desc_sw128(b_addr + k * 2048, BK * 128, 1024);
-                            if constexpr (Cfg::CG == 2)
-                                umma_f16_ss_pair(d_tmem, ad, bd, idesc, (first && k == 0) ? 0u : 1u);
-                            else
-                                umma_f16_ss(d_tmem, ad, bd, idesc, (first && k == 0) ? 0u : 1u);
+                        for (int q = 0; q < Cfg::KSUB; ++q) {
+                            // a sub-tile wholly beyond K holds only zero fill
+                            if (q > 0 && kt * Cfg::SBK + q * BK >= args.K) break;
+                            const uint32_t a_addr = smem_u32(sA + s * Cfg::A_BYTES + q * Cfg::A_SUB);
+                            const uint32_t b_addr = smem_u32(sB + s * Cfg::B_BYTES + q * Cfg::B_SUB);
+#pragma unroll
+                            for (int k = 0; k < BK / 16; ++k) {
+                                const uint64_t ad = smem_desc_sw128(a_addr + k * 32, 16, 1024);
+                                const uint64_t bd =
+                                    smem_desc_sw128(b_addr + k * 2048, BK * 128, 1024);
+                                const uint32_t acc = (first && q == 0 && k == 0) ? 0u : 1u;
+                                if constexpr (Cfg::CG == 2)
+                                    umma_f16_ss_pair(d_tmem, ad, bd, idesc, acc);
+                                else
+                                    umma_f16_ss(d_tmem, ad, bd, idesc, acc);
+                            }
                         }
                         // stage s is free once these MMAs have read it (in both CTAs
                         // of a pair)
@@ -1174,7 +1202,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 // end).  Longer rounds (up to 1024 products, |x| <= 2^24) use
                 // the exact float-to-int conversion, which is slower per value
                 // but needed 4x less often.
-                constexpr bool kMagicFold = Cfg::KC * Cfg::BK <= 256;
+                constexpr bool kMagicFold = Cfg::KC * Cfg::SBK <= 256;
                 constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
                 uint32_t acc[Cfg::EPI_COLS];
 #pragma unroll
@@ -1330,7 +1358,7 @@ static cudaError_t launch_tc(const P &p, cudaStream_t stream) {
     a.K = p.K;
     a.num_m_tiles = (p.M + Cfg::BM - 1) / Cfg::BM;
     a.num_n_tiles = (p.N + Cfg::BN - 1) / Cfg::BN;
-    a.num_k_tiles = (p.K + Cfg::BK - 1) / Cfg::BK;
+    a.num_k_tiles = (p.K + Cfg::SBK - 1) / Cfg::SBK;
     // groups of 8 tile rows: bf16 8192^3 reads 1107 MB from DRAM against 1247
     // with 16 (and 1614 with 4), and runs about 1 % faster
     a.group_m = p.group_m > 0 ? p.group_m : 8;
@@ -1453,7 +1481,7 @@ static KernelInfo tc_info() {
     KernelInfo k;
     k.bm = Cfg::BM * Cfg::CM;  // the tile a cluster computes
     k.bn = Cfg::BN;
-    k.bk = Cfg::BK;
+    k.bk = Cfg::SBK;  // K columns per stage
     k.stages = Cfg::STAGES;
     k.threads = Cfg::THREADS;
     k.smem_bytes = Cfg::SMEM_BYTES;

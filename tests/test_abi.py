@@ -58,7 +58,13 @@ def test_list_configs(L):
     assert {c[3] for c in bf16 if c[1] == 128} == {1, 2, 3, 4, 5, 6}
     # 128 x 256 single-CTA tiles fit four stages; the CTA pair's 256 x 256 six
     assert {c[3] for c in bf16 if c[1] == 256 and c[0] == 128} == {1, 2, 3, 4}
-    assert {c[3] for c in bf16 if c[0] == 256} == {4, 5, 6}
+    assert {c[3] for c in bf16 if c[0] == 256 and c[2] == 64} == {4, 5, 6}
+    # the pair also with stages of 128 K columns (two 64-column sub-tiles
+    # landed under one barrier), TMA producer, for both tensor-core dtypes
+    for cfgs in (bf16, i8):
+        wide = [c for c in cfgs if c[0] == 256 and c[2] == 128]
+        assert {c[3] for c in wide} == {2, 3}
+        assert all(len(c) <= 5 or c[5] == pg.PRODUCERS["tma"] for c in wide)
     # the register-staged comparator: fp32 only, two buffers, named by its producer
     regs = [c for c in f32 if len(c) > 5 and c[5] == pg.PRODUCERS["registers"]]
     assert {(c[0], c[1], c[3]) for c in regs} == {(128, 128, 2), (128, 64, 2)}

@@ -21,20 +21,22 @@ def sms():
     return torch.cuda.get_device_properties(0).multi_processor_count
 
 
+# (bm, bn, bk, stages); the CTA pair's stages hold 128 K columns each
 @pytest.mark.parametrize("dtype,M,N,K,expect", [
-    ("f32", 4096, 4096, 4096, (128, 128, 3)),
-    ("f32", 8192, 8192, 8192, (128, 128, 3)),
-    ("f32", 256, 256, 256, (128, 64, 3)),      # 4 tiles of 128 x 128: too few for two per SM
-    ("bf16", 8192, 8192, 8192, (256, 256, 6)),
-    ("i8", 4096, 4096, 4096, (256, 256, 6)),
-    ("bf16", 4096, 4096, 2048, (256, 256, 6)),
-    ("bf16", 4096, 4096, 128, (128, 128, 4)),  # K <= 128: bound by writing C
-    ("i8", 4096, 4096, 32, (128, 128, 4)),
-    ("bf16", 2048, 2048, 8192, (128, 128, 4)),  # 64 pair tiles: fewer than half the SMs
-    ("bf16", 1024, 1024, 16384, (128, 128, 4)),
+    ("f32", 4096, 4096, 4096, (128, 128, 32, 3)),
+    ("f32", 8192, 8192, 8192, (128, 128, 32, 3)),
+    ("f32", 256, 256, 256, (128, 64, 32, 3)),      # 4 tiles of 128 x 128: too few for two per SM
+    ("bf16", 8192, 8192, 8192, (256, 256, 128, 3)),
+    ("i8", 4096, 4096, 4096, (256, 256, 128, 3)),
+    ("bf16", 4096, 4096, 2048, (256, 256, 128, 3)),
+    ("bf16", 4096, 4096, 256, (256, 256, 128, 3)),
+    ("bf16", 4096, 4096, 128, (128, 128, 64, 4)),  # K <= 128: bound by writing C
+    ("i8", 4096, 4096, 32, (128, 128, 64, 4)),
+    ("bf16", 2048, 2048, 8192, (128, 128, 64, 4)),  # 64 pair tiles: fewer than half the SMs
+    ("bf16", 1024, 1024, 16384, (128, 128, 64, 4)),
 ])
 def test_default_table(dtype, M, N, K, expect):
     if sms() != 152:
         pytest.skip("the expectations are written for 152 SMs")
     cfg = pg.pgemm_default_config(dtype, M, N, K)
-    assert (cfg[0], cfg[1], cfg[3]) == expect, cfg
+    assert tuple(cfg[:4]) == expect, cfg

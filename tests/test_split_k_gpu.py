@@ -70,15 +70,15 @@ def check(orc, dtype, M, N, K, seed, kind="random", alpha=1, beta=0, config=None
     return got
 
 
-# 1000 x 1000 x 4100: fewer tiles than slots for every configuration, so every
-# element of C comes from stream-K pieces: with the cap at 8, 65 K-tiles in
-# ranges of 13 to 27, up to six pieces a tile, the last piece of a tile
-# ending on the ragged 65th K-tile; with the default cap, equal halves (65
-# K-tiles: too many for half-width units).  Bit-exact against the oracle on
+# 1000 x 1000 x 8200: fewer tiles than slots for every configuration, so every
+# element of C comes from stream-K pieces: with the cap at 8, 129 K-tiles of
+# 64 columns (65 of 128) in ranges of 13 to 55, up to six pieces a tile, the
+# last piece of a tile ending on the ragged last K-tile; with the default
+# cap, equal halves (K beyond 2048 columns: no half-width units).  Bit-exact against the oracle on
 # sampled entries and against the same call without stream-K on all of C.
 @pytest.mark.parametrize("dtype", ["bf16", "i8"])
 def test_every_config_stream_k_exactly(orc, dtype):
-    M, N, K = 1000, 1000, 4100
+    M, N, K = 1000, 1000, 8200
     A, B, C = operands(dtype, M, N, K, si.config_seed(20, 1 if dtype == "i8" else 2), "int")
     one = 1 if dtype == "i8" else 1.0
     zero = 0 if dtype == "i8" else 0.0
@@ -176,7 +176,7 @@ def test_int8_exchange_stress(orc):
 def test_full_size_defaults_split():
     """The bench's tensor-core workloads deal their leftover tiles out along K
     (on 152 SMs: 28 of int8 4096^3's 256 pair tiles, 36 of bf16 8192^3's
-    1024); bf16 with K of at most 32 K-tiles cuts them into half-width units
+    1024); bf16 with K of at most 2048 columns cuts them into half-width units
     (the exact-int8 kernels have no half-width units)."""
     for dtype, n in (("i8", 4096), ("bf16", 8192)):
         s = pg.pgemm_schedule(dtype, n, n, n)
@@ -190,14 +190,15 @@ def test_full_size_defaults_split():
     assert s["half_tiles"] == 0 and s["split_tiles"] > 0, s
 
 
-# Half-width units (K of at most 32 K-tiles): bit-exact on integer-valued
+# Half-width units (K of at most 2048 columns): bit-exact on integer-valued
 # operands against the oracle and the unsplit call, on shapes whose last tile
 # column is ragged (N = 1000: the right half of the last column partly beyond
 # N; N = 320: entirely beyond), with beta != 0 (only the computed half's
 # columns read C) and a ragged last K-tile.
 @pytest.mark.parametrize("dtype", ["bf16"])
 @pytest.mark.parametrize("M,N,K", [(1000, 1000, 2000), (700, 320, 1000), (2560, 2560, 1984)])
-@pytest.mark.parametrize("cfg", [(256, 256, 64, 6), (256, 256, 64, 4), (128, 256, 64, 4)])
+@pytest.mark.parametrize("cfg", [(256, 256, 128, 3), (256, 256, 64, 6), (256, 256, 64, 4),
+                                 (128, 256, 64, 4)])
 def test_half_width_units(orc, dtype, M, N, K, cfg):
     s = pg.pgemm_schedule(dtype, M, N, K, cfg)
     assert s["half_tiles"] > 0 and s["split_tiles"] == 0, s
