@@ -232,16 +232,25 @@ __device__ __forceinline__ void store_block32(const GemmArgs<Scalar, Scalar> &a,
                    have_acc ? vals[4 * j + 3] : z);
         }
         __syncwarp();
-        const bool read_c = a.beta != Scalar(0);
+        // the block's rows inside C (none when m_base >= M) and this lane's column
+        const int rows = a.M - m_base < 32 ? a.M - m_base : 32;
         const int c = col + static_cast<int>(lane);
+        if (c < a.N) {
+            Scalar *cp = a.C + static_cast<long long>(m_base) * a.ldc + c;
+            const uint32_t rd = sbuf + (lane & 3) * 4;
+            const uint32_t ch = lane >> 2;
+            if (a.beta != Scalar(0)) {
 #pragma unroll 4
-        for (int r = 0; r < 32; ++r) {
-            const uint32_t w = lds32(sbuf + r * 128 + ((((lane >> 2) ^ (r & 7))) << 4) + (lane & 3) * 4);
-            const int row = m_base + r;
-            if (row < a.M && c < a.N) {
-                Scalar *cp = a.C + static_cast<long long>(row) * a.ldc + c;
-                const Scalar x = __builtin_bit_cast(Scalar, w);
-                *cp = read_c ? axpby(a.alpha, x, a.beta, *cp) : axpby(a.alpha, x, Scalar(0), Scalar(0));
+                for (int r = 0; r < rows; ++r, cp += a.ldc) {
+                    const uint32_t w = lds32(rd + r * 128 + ((ch ^ (r & 7)) << 4));
+                    *cp = axpby(a.alpha, __builtin_bit_cast(Scalar, w), a.beta, *cp);
+                }
+            } else {
+#pragma unroll 4
+                for (int r = 0; r < rows; ++r, cp += a.ldc) {
+                    const uint32_t w = lds32(rd + r * 128 + ((ch ^ (r & 7)) << 4));
+                    *cp = axpby(a.alpha, __builtin_bit_cast(Scalar, w), Scalar(0), Scalar(0));
+                }
             }
         }
         __syncwarp();
