@@ -756,8 +756,9 @@ def main():
                            "shape": [r["M"], r["N"], r["K"]],
                            "ms_per_step": round(r["ms_per_step"], 4),
                            "ms_median": round(r["ms_median"], 4),
-                           "roofline": roofline_point(r["dtype"], r["M"], r["N"], r["K"], r["beta"],
-                                                      r["ms_per_step"], sm_count, peaks),
+                           "roofline": {**roofline_point(r["dtype"], r["M"], r["N"], r["K"], r["beta"],
+                                                         r["ms_per_step"], sm_count, peaks),
+                                        "traffic": traffic_for(other)},
                            "config": r["config"]}
 
     cpu = None
