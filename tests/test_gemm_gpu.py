@@ -176,6 +176,36 @@ def test_every_config_every_tile_count(orc, dtype):
                       config=cfg)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "i8"])
+def test_two_subtile_stages_ragged_k(orc, dtype):
+    """Stages of 128 K columns land two 64-column sub-tiles under one barrier.
+    In the last stage a sub-tile that starts at or beyond K is neither loaded
+    nor multiplied (K mod 128 in [1, 64]), one that starts below K is
+    zero-filled past it (K mod 128 in [65, 127]); exact on integer operands."""
+    cfgs = [c for c in _configs(dtype) if c[0] == 256 and c[2] == 128]
+    assert cfgs
+    for cfg in cfgs:
+        for K in (1, 63, 64, 65, 127, 129, 3 * 128 + 1, 3 * 128 + 64, 3 * 128 + 100, 1024 + 64):
+            check(orc, dtype, 300, 520, K, 1, 0, seed=7500 + K + cfg[3],
+                  kind="random" if dtype == "i8" else "int", config=cfg)
+
+
+@pytest.mark.parametrize("K", [1024, 1025, 2048 + 64, 4096])
+def test_int8_extremes_on_two_subtile_stages(orc, K):
+    """The exact rounds of 1024 products are eight 128-column stages: a round
+    boundary, one column past it, and a ragged last stage, at the products'
+    extremes."""
+    M, N = 300, 520
+    for cfg in [c for c in _configs("i8") if c[0] == 256 and c[2] == 128]:
+        for a, b in ((-128, -128), (127, -128)):
+            A = np.full((M, K), a, np.int8)
+            B = np.full((K, N), b, np.int8)
+            C = np.zeros((M, N), np.int32)
+            got, status = run_gpu("i8", A, B, C, 1, 0, config=cfg)
+            assert status == 0
+            assert np.all(got == np.int32(K * a * b)), (cfg, K, a, b)
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32", "i8"])
 def test_persistent_multi_tile_per_block(orc, dtype):
     """More output tiles than resident blocks: each block runs several tiles
