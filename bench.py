@@ -516,6 +516,7 @@ def run_point(dtype, M, N, K, recipe, cfg, steps, warmup, seed=None):
             "stages": cfg[3], "max_k_parts": cfg[4] if len(cfg) > 4 else 0,
             "group_m": cfg[7] if len(cfg) > 7 else 0,
             "producer": {v: k for k, v in pg.PRODUCERS.items()}[cfg[5] if len(cfg) > 5 else 0],
+            "engine": {v: k for k, v in pg.ENGINES.items()}[cfg[6] if len(cfg) > 6 else 0],
             "k_tiles": -(-K // cfg[2]), **attrs, **sched, "ms_median": round(med, 4),
             "ms_min": round(min(ms), 4), "tflops": round(flops / (med * 1e-3) / 1e12, 2),
             "gbs": round((in_bytes + out_bytes) / (med * 1e-3) / 1e9, 1), "status": status}
