@@ -550,8 +550,6 @@ __device__ __forceinline__ void widen_box(const TcOperands &op, const WidenBoxes
     for (int j = 0; j < 4; ++j) {
         const uint32_t p = t + 128u * j;  // 16-byte piece of the box
         int r, cx;                        // row and column (bytes) of the piece in the matrix
-        const int8_t *unused = nullptr;
-        (void)unused;
         if (is_a) {  // 128 rows of 64 bytes: 4 pieces a row
             r = y + static_cast<int>(p >> 2);
             cx = x + static_cast<int>(p & 3u) * 16;
