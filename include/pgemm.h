@@ -137,7 +137,7 @@ typedef enum { PGEMM_ENGINE_DEFAULT = 0, PGEMM_ENGINE_MMA_SYNC = 1 } pgemm_engin
  * the other fields set means "whichever built K-tile matches".  The CTA pair
  * (bm = bn = 256) is built with 64-column stages (S = 4..6) and with 128-column
  * stages (bk = 128, S = 2 or 3: two 64-column sub-tiles landed under one
- * barrier, the default for bf16 and int8 pairs). */
+ * barrier, the default for bf16 and int8 pairs).
  *
  * max_k_parts (the pages have no counterpart): stream-K against wave
  * quantisation (pgemm_stream_k_plan).  The tiles a partial last wave would
