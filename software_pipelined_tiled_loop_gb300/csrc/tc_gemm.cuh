@@ -1366,9 +1366,13 @@ static cudaError_t launch_tc(const P &p, cudaStream_t stream) {
     a.num_m_tiles = (p.M + Cfg::BM - 1) / Cfg::BM;
     a.num_n_tiles = (p.N + Cfg::BN - 1) / Cfg::BN;
     a.num_k_tiles = (p.K + Cfg::SBK - 1) / Cfg::SBK;
-    // groups of 8 tile rows: bf16 8192^3 reads 1107 MB from DRAM against 1247
-    // with 16 (and 1614 with 4), and runs about 1 % faster
-    a.group_m = p.group_m > 0 ? p.group_m : 8;
+    // Raster groups of 16 tile rows up to K = 4096, else 8.  On the pair
+    // with 128-column stages: int8 4096^3 100.1-100.4 us with 16 against
+    // 101.1-102.0 with 8, bf16 4096^3 86.0-87.1 against 86.9-88.1; bf16
+    // 4096^2 x 16384 304.2-306.2 us with 8 against 309.3-310.5 with 16 (a
+    // group of 16 pair rows then holds 128 MiB of A); bf16 8192^3 the same
+    // time with 8 or 16 and 1063 against 1253 MB read from DRAM with 8.
+    a.group_m = p.group_m > 0 ? p.group_m : (p.K <= 4096 ? 16 : 8);
     a.alpha = p.alpha;
     a.beta = p.beta;
     a.C = p.C;
