@@ -168,24 +168,37 @@ static const KernelInfo *table_of(pgemm_dtype dt, int *count) {
 //  * fp32: 128 x 128 tiles with three stages (two blocks per SM; four or more
 //    stages drop to one block per SM and lose 16 %); 128 x 64 tiles when the
 //    128 x 128 grid would leave SMs without two blocks each.
-//  * bf16 and int8: 256 x 256 tiles on a CTA pair (cta_group::2) when the
+//  * bf16 and int8, short K (bf16 K <= 384, int8 K <= 512) when 128 x 256
+//    tiles fill at least three waves: 128 x 256 tiles, three stages up to
+//    K = 128, else four.  There the call is bound by writing C and by each
+//    tile's fixed hand-offs (load, MMA, accumulator, epilogue), and the wider
+//    tile halves the hand-offs for the same C bytes per SM (4096^2, mean of
+//    200 calls: bf16 K = 32 16.4 against 18.4 us with 128 x 128, K = 64 16.5
+//    against 16.8, K = 192 18.7 against 22.5 with the pair, K = 256 20.6
+//    against 22.6, K = 384 level; int8 K = 32 27.6 against 32.8, K = 256
+//    29.7 against 33.7, K = 512 32.8 against 35.9).  With fewer waves the
+//    last wave's larger stores cost more than that (bf16 2048 x 4096 x 32:
+//    12.4 against 12.9 us for 128 x 128).
+//  * otherwise 256 x 256 tiles on a CTA pair (cta_group::2) when the
 //    pairs cover half the SMs (bf16 8192^3 +12 %, int8 4096^3 +10 % over
 //    128 x 256), with three stages of 128 K columns, each landed as two
 //    64-column sub-tiles under one barrier: the MMA warp then waits, commits
 //    and loops once per 8 MMAs instead of 4 (against six 64-column stages in
 //    the same shared memory: bf16 4096^2 x 512 -8 %, x 2048 -4 %, 8192^3
-//    -1 %, int8 4096^3 -1 %); else 128 x 128.  (128 x 256 tiles never
-//    win the choice: a grid has at most twice as many of them as pair
-//    tiles, so whenever they would cover every SM the pairs cover half.)  At
-//    most two K-tiles (K <= 128): the call is bound by writing C, and 128 x
-//    128 tiles with four stages (room for two epilogue staging buffers per
-//    warp) write it fastest.
+//    -1 %, int8 4096^3 -1 %); else 128 x 128 with four stages.
 static pgemm_config default_config(pgemm_dtype dt, int M, int N, int K, int sm_count) {
     pgemm_config c{128, 128, 0, 4};
     if (dt == PGEMM_F32) {
         const long long tiles128 = (long long)((M + 127) / 128) * ((N + 127) / 128);
         c.bn = tiles128 >= 2LL * sm_count ? 128 : 64;
         c.stages = 3;
+        return c;
+    }
+    const long long wide_tiles = (long long)((M + 127) / 128) * ((N + 255) / 256);
+    const int wide_max_k = dt == PGEMM_I8 ? 512 : 384;
+    if (K <= wide_max_k && wide_tiles >= 3LL * sm_count) {
+        c.bn = 256;
+        c.stages = K <= 128 ? 3 : 4;
         return c;
     }
     const long long pairs = (long long)((M + 255) / 256) * ((N + 255) / 256);

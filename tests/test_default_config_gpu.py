@@ -29,9 +29,17 @@ def sms():
     ("bf16", 8192, 8192, 8192, (256, 256, 128, 3)),
     ("i8", 4096, 4096, 4096, (256, 256, 128, 3)),
     ("bf16", 4096, 4096, 2048, (256, 256, 128, 3)),
-    ("bf16", 4096, 4096, 256, (256, 256, 128, 3)),
-    ("bf16", 4096, 4096, 128, (128, 128, 64, 4)),  # K <= 128: bound by writing C
-    ("i8", 4096, 4096, 32, (128, 128, 64, 4)),
+    ("bf16", 4096, 4096, 512, (256, 256, 128, 3)),
+    # short K, 128 x 256 tiles filling three waves: bound by writing C
+    ("bf16", 4096, 4096, 128, (128, 256, 64, 3)),
+    ("bf16", 4096, 4096, 256, (128, 256, 64, 4)),
+    ("bf16", 4096, 4096, 384, (128, 256, 64, 4)),
+    ("i8", 4096, 4096, 32, (128, 256, 64, 3)),
+    ("i8", 4096, 4096, 512, (128, 256, 64, 4)),
+    ("i8", 4096, 4096, 1024, (256, 256, 128, 3)),
+    # fewer than three waves of 128 x 256 tiles: 128 x 128
+    ("bf16", 2048, 4096, 32, (128, 128, 64, 4)),
+    ("bf16", 1024, 1024, 64, (128, 128, 64, 4)),
     ("bf16", 2048, 2048, 8192, (128, 128, 64, 4)),  # 64 pair tiles: fewer than half the SMs
     ("bf16", 1024, 1024, 16384, (128, 128, 64, 4)),
 ])
