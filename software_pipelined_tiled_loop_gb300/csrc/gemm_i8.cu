@@ -86,7 +86,10 @@ struct WidenJob {
     __half *dst;
     long long dld;   // destination pitch (elements)
     int rows, cols;
-    int vec;         // 1: 16-byte vectors (aligned rows, cols % 16 == 0)
+    int vec;         // 1: 16-byte vectors (aligned rows, cols % 16 == 0);
+                     // 2: the same for rows of fewer than 512 groups of 8,
+                     //    walked flat (rows * groups < 2^30, so that a
+                     //    thread's 32-bit index cannot overflow)
 };
 
 // dst[r][c] = (fp16) src[r][c] for r < rows, c < cols, for the two operands
@@ -97,10 +100,14 @@ struct WidenJob {
 // kWidenGroups groups of every row before converting any, keeping
 // kWidenRows * kWidenGroups independent loads in flight: one dependent load
 // per thread at a time covers only a fraction of the latency-bandwidth
-// product.  The fp16 output is written back through L2, where the GEMM that
+// product.  Rows of fewer than blockDim * kWidenGroups groups (under 4096
+// columns) would leave threads of that walk idle, so there the threads take
+// the operand's (row, group) pairs in one flat sequence instead, each
+// kWidenFlat of them in flight.  The fp16 output is written back through L2, where the GEMM that
 // follows finds most of it.
 constexpr int kWidenRows = 2;
 constexpr int kWidenGroups = 2;
+constexpr int kWidenFlat = 4;
 
 __global__ void __launch_bounds__(256, 6) widen_i8_to_f16_kernel(WidenJob ja, WidenJob jb,
                                                                  uint32_t *zero, int zero_words) {
@@ -110,7 +117,38 @@ __global__ void __launch_bounds__(256, 6) widen_i8_to_f16_kernel(WidenJob ja, Wi
         for (int i = threadIdx.x; i < zero_words; i += blockDim.x) zero[i] = 0u;
     const WidenJob &j = blockIdx.y == 0 ? ja : jb;
     if (j.rows <= 0 || j.cols <= 0) return;
-    if (j.vec) {
+    if (j.vec == 2) {
+        // narrow rows: flat over (row, group), consecutive threads on
+        // consecutive groups of a row and then of the next row (rows x
+        // groups < 2^30 on this path: 32-bit indices)
+        const int groups = j.cols / 8;
+        const int total = j.rows * groups;
+        const int stride = static_cast<int>(gridDim.x * blockDim.x);
+        for (int i0 = static_cast<int>(blockIdx.x * blockDim.x + threadIdx.x); i0 < total;
+             i0 += stride * kWidenFlat) {
+            uint2 w[kWidenFlat];
+#pragma unroll
+            for (int u = 0; u < kWidenFlat; ++u) {
+                const int i = i0 + u * stride;
+                if (i < total) {
+                    const int r = i / groups;
+                    w[u] = __ldg(reinterpret_cast<const uint2 *>(j.src + r * j.sld) + (i - r * groups));
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kWidenFlat; ++u) {
+                const int i = i0 + u * stride;
+                if (i < total) {
+                    const int r = i / groups;
+                    __half2 o[4];
+                    widen4(w[u].x, o[0], o[1]);
+                    widen4(w[u].y, o[2], o[3]);
+                    reinterpret_cast<uint4 *>(j.dst + r * j.dld)[i - r * groups] =
+                        *reinterpret_cast<const uint4 *>(o);
+                }
+            }
+        }
+    } else if (j.vec) {
         const int groups = j.cols / 8;  // cols % 16 == 0 on this path
         const int step = static_cast<int>(blockDim.x) * kWidenGroups;
         for (long long r0 = static_cast<long long>(blockIdx.x) * kWidenRows; r0 < j.rows;
@@ -160,6 +198,9 @@ static WidenJob make_job(const int8_t *src, long long sld, void *dst, long long 
              (reinterpret_cast<uintptr_t>(dst) & 15u) == 0 && dld % 8 == 0 && cols % 16 == 0)
                 ? 1
                 : 0;
+    if (j.vec && cols / 8 < 256 * kWidenGroups &&
+        static_cast<long long>(rows) * (cols / 8) < (1LL << 30))
+        j.vec = 2;
     return j;
 }
 
@@ -173,8 +214,11 @@ cudaError_t launch_widen_i8_pair(const int8_t *a, long long lda, void *a_dst, lo
     // vector path: one block per kWidenRows rows; scalar path: about four
     // values per thread
     auto blocks_for = [](const WidenJob &j) -> long long {
-        return j.vec ? (static_cast<long long>(j.rows) + kWidenRows - 1) / kWidenRows
-                     : (static_cast<long long>(j.rows) * j.cols + 1023) / 1024;
+        if (!j.vec) return (static_cast<long long>(j.rows) * j.cols + 1023) / 1024;
+        if (j.vec == 2)  // flat walk: kWidenFlat groups a thread
+            return (static_cast<long long>(j.rows) * (j.cols / 8) + 256 * kWidenFlat - 1) /
+                   (256 * kWidenFlat);
+        return (static_cast<long long>(j.rows) + kWidenRows - 1) / kWidenRows;
     };
     long long blocks = blocks_for(ja) > blocks_for(jb) ? blocks_for(ja) : blocks_for(jb);
     const long long cap = static_cast<long long>(sm_count) * 16;
