@@ -123,6 +123,14 @@ def test_int8_4096_each_tile(orc, bn):
     check_sampled(orc, "i8_uniform", 4096, 4096, 4096, si.config_seed(3), config=(128, bn, 64, 4))
 
 
+@pytest.mark.parametrize("K", [32, 256, 512])
+def test_int8_4096_short_k_default(orc, K):
+    """Short-K int8 at 4096^2 takes the default 128 x 256 tiles and the flat
+    widening walk (rows of A under 4096 columns); whole matrix, bit-exact."""
+    assert pg.pgemm_default_config("i8", 4096, 4096, K)[:2] == (128, 256)
+    check_full(orc, "i8_uniform", 4096, 4096, K, si.config_seed(3, K))
+
+
 def test_bf16_8192(orc):
     check_sampled(orc, "bf16_normal", 8192, 8192, 8192, si.config_seed(4))
 
