@@ -296,17 +296,20 @@ def run_e2e(torch, fn, dtype, M, N, K, alpha, beta, A, B, C0, dA, dB, dC, e_step
     from pinned host memory to the device, runs the GEMM and reads C back.
 
     The steps are software-pipelined across streams the way the kernel
-    pipelines its K-loop: two device buffer sets, host-to-device copies on one
-    copy stream, the GEMM on the compute stream, the read-back on another, so
-    that step i's copies overlap step i - 1's GEMM.  A step's copies into a
-    buffer set wait until the step two before it has read its result back
-    from that set.  The serial loop (copy, GEMM, read back, one after
+    pipelines its K-loop: three device buffer sets, host-to-device copies on
+    one copy stream, the GEMM on the compute stream, the read-back on
+    another, so that step i's copies overlap step i - 1's GEMM.  A step's
+    copies into a buffer set wait until the step three before it has read its
+    result back from that set (with two sets, a copy held up behind the
+    previous read-back held up the next GEMM).  The serial loop (copy, GEMM, read back, one after
     another) is timed too and reported beside it."""
     hA = torch.from_numpy(A.view(np.int16) if A.dtype == np.uint16 else A).pin_memory()
     hB = torch.from_numpy(B.view(np.int16) if B.dtype == np.uint16 else B).pin_memory()
     hC = torch.from_numpy(C0).pin_memory()
-    hOut = [torch.empty_like(hC).pin_memory() for _ in range(2)]
-    sets = [(dA, dB, dC), (torch.empty_like(dA), torch.empty_like(dB), torch.empty_like(dC))]
+    NSETS = 3
+    hOut = [torch.empty_like(hC).pin_memory() for _ in range(NSETS)]
+    sets = [(dA, dB, dC)] + [(torch.empty_like(dA), torch.empty_like(dB), torch.empty_like(dC))
+                             for _ in range(NSETS - 1)]
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
 
     def serial(n):
@@ -321,10 +324,10 @@ def run_e2e(torch, fn, dtype, M, N, K, alpha, beta, A, B, C0, dA, dB, dC, e_step
         s_in.wait_event(t0)
         read_back = []
         for i in range(n):
-            a, b, c = sets[i % 2]
+            a, b, c = sets[i % NSETS]
             with torch.cuda.stream(s_in):
-                if i >= 2:
-                    s_in.wait_event(read_back[i - 2])
+                if i >= NSETS:
+                    s_in.wait_event(read_back[i - NSETS])
                 a.copy_(hA, non_blocking=True)
                 b.copy_(hB, non_blocking=True)
                 c.copy_(hC, non_blocking=True)
@@ -336,7 +339,7 @@ def run_e2e(torch, fn, dtype, M, N, K, alpha, beta, A, B, C0, dA, dB, dC, e_step
             done.record(stream)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(done)
-                hOut[i % 2].copy_(c, non_blocking=True)
+                hOut[i % NSETS].copy_(c, non_blocking=True)
                 back = torch.cuda.Event()
                 back.record(s_out)
             read_back.append(back)
@@ -362,7 +365,7 @@ def run_e2e(torch, fn, dtype, M, N, K, alpha, beta, A, B, C0, dA, dB, dC, e_step
         timed(body, 2)
     ms_serial = timed(serial, e_steps)
     ms_pipe = timed(pipelined, e_steps)
-    for h in hOut:  # both read-back buffers hold a full result
+    for h in hOut:  # every read-back buffer holds a full result
         if not torch.equal(h, hOut[0]):
             raise RuntimeError("pipelined read-back differs between buffer sets")
     tput = lambda ms: round(flops * e_steps * dist_ctx.world / (ms * 1e-3) / 1e12, 3)
@@ -370,7 +373,7 @@ def run_e2e(torch, fn, dtype, M, N, K, alpha, beta, A, B, C0, dA, dB, dC, e_step
     return {"value": tput(ms_pipe), "unit": "TFLOP/s" if dtype != "i8" else "TOP/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(C0.nbytes),
             "steps": e_steps, "ms_per_step": round(ms_pipe / e_steps, 4),
-            "pipelined": "two buffer sets; copies overlap the neighbouring steps' GEMMs",
+            "pipelined": "three buffer sets; copies overlap the neighbouring steps' GEMMs",
             "serial_value": tput(ms_serial), "serial_ms_per_step": round(ms_serial / e_steps, 4)}
 
 
